@@ -1,0 +1,466 @@
+"""Benchmark of the balanced expert-parallel dispatch hot path on one GB300.
+
+One step = one pass of the whole path over one batch at the bench-shaped
+training workload (R=8 virtual ranks, S=8192 tokens/rank, E=384, K=8,
+H=7168, H'=2048, B=48):
+    plan -> prefetch_weight -> dispatch -> grouped GEMM -> combine
+    -> combine backward (dY) -> reduce_grad (replica grads into home rows).
+The K timed steps cycle through four routings tuned to maxvio 0.2 / 1 / 10 / 20
+(all resident in HBM), so the job spans the skew range; per-maxvio times are
+reported under "sweep". Inputs (tens of GB) are far larger than L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bep|reference]
+
+--impl reference times the CPU oracle (the slow plain restatement) on a bounded
+sample of the same workload. Under torchrun (N > 1) every rank runs an
+independent replica of the job on its own GPU (the path has no cross-GPU
+exchange on one GPU: replicas only); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "bench_r8_e384"
+TARGETS = (0.2, 1.0, 10.0, 20.0)
+METRIC = "dispatch+combine tokens/s and HBM GB/s vs peak, maxvio 0.2-20, 1 GB300"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bep_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    s, m = float(parts[0]), float(parts[1])
+                except ValueError:
+                    continue
+                sm.append(s)
+                mx.append(m)
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import moe_expert_dispatch_online_gb300 as bep
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = synth.WORKLOADS[args.workload]
+    R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+    cfg = bep.Config(R, E, B, K, S, H, Hp, wl.mode)
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, dev, with_grad=True)
+
+    targets = TARGETS if args.workload == WORKLOAD else synth.MAXVIO_TARGETS[args.workload]
+    topks = [torch.from_numpy(synth.routing(wl, t, 0)).to(dev) for t in targets]
+    x = synth.tokens_device((R, S, H), 1, device=dev)
+    gates = torch.from_numpy(synth.gates_host(R, S, K, 1)).to(dev)
+    dout = synth.tokens_device((R, S, Hp), 2, device=dev)
+    w_home = synth.weights_device((E, H, Hp), 3, device=dev)
+    w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=dev)
+    g_home = torch.zeros((E, H, Hp), dtype=torch.float32, device=dev)
+    red = torch.empty((R, B, H, Hp), dtype=torch.float32, device=dev)
+    red.normal_(0.0, 1e-3)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    stages = ("plan", "prefetch", "dispatch", "gemm", "combine", "combine_bwd", "reduce_grad")
+
+    def step(i, ev=None):
+        topk = topks[i % len(topks)]
+        if ev is not None:
+            ev[0].record(stream)
+        bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+        if ev is not None:
+            ev[5].record(stream)
+        bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream)
+        if ev is not None:
+            ev[6].record(stream)
+        bep.bep_reduce_grad(ctx, buf.slot_expert, g_home, red, stream)
+        if ev is not None:
+            ev[7].record(stream)
+
+    # per-step statistics that do not depend on timing
+    maxvios, nrep = [], []
+    for i in range(len(topks)):
+        step(i)
+        torch.cuda.synchronize()
+        maxvios.append(float(buf.maxvio.item()))
+        nrep.append(int((buf.slot_expert >= 0).sum().item()))
+    st = bep.bep_status(ctx, stream)
+    if st:
+        raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = {s: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+                for j, s in enumerate(stages)}
+    st = bep.bep_status(ctx, stream)
+    if st:
+        raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+
+    # ---- end to end through the public API with host buffers
+    x_h = x.cpu().pin_memory()
+    dout_h = dout.cpu().pin_memory()
+    gates_h = gates.cpu().pin_memory()
+    topks_h = [t.cpu().pin_memory() for t in topks]
+    out_h = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    topk_d = torch.empty_like(topks[0])
+    h2d = x_h.numel() * 2 + dout_h.numel() * 2 + gates_h.numel() * 4 + topks_h[0].numel() * 4
+    d2h = out_h.numel() * 2
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            topk_d.copy_(topks_h[i % len(topks_h)], non_blocking=True)
+            x.copy_(x_h, non_blocking=True)
+            gates.copy_(gates_h, non_blocking=True)
+            dout.copy_(dout_h, non_blocking=True)
+        bep.bep_plan(ctx, topk_d, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
+        bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+        bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+        bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
+        bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+        bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream)
+        bep.bep_reduce_grad(ctx, buf.slot_expert, g_home, red, stream)
+        with torch.cuda.stream(stream):
+            out_h.copy_(buf.out, non_blocking=True)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    dist_barrier(world)
+
+    total_ms = dist_max(world, total_ms)
+    e2e_ms = dist_max(world, e2e_ms)
+    tokens_per_step = R * S
+    pk = peaks()
+    gemm_ms = statistics.mean(stage_ms["gemm"])
+    gemm_flops = 2.0 * R * S * K * H * Hp
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    # algorithmic HBM bytes of the memory-bound stages
+    row_h, row_hp = H * 2, Hp * 2
+    disp_bytes = R * S * row_h + R * S * K * row_h + R * S * K * 4
+    comb_bytes = R * S * K * row_hp + R * S * row_hp + R * S * K * 8
+    disp_ms = statistics.mean(stage_ms["dispatch"])
+    comb_ms = statistics.mean(stage_ms["combine"])
+    per_target = {}
+    for j, t in enumerate(targets):
+        idx = [i for i in range(args.steps) if i % len(targets) == j]
+        if not idx:
+            continue
+        step_ms = [sum(stage_ms[s][i] for s in stages) for i in idx]
+        per_target[f"{t:g}"] = {
+            "maxvio": round(maxvios[j], 4), "replicas": nrep[j],
+            "step_ms": round(statistics.mean(step_ms), 4),
+            **{f"{s}_ms": round(statistics.mean(stage_ms[s][i] for i in idx), 4) for s in stages},
+        }
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(f"grouped_gemm|{args.workload}")
+    clocks = clk.summary()
+    result = {
+        "metric": METRIC,
+        "value": world * tokens_per_step * args.steps / (total_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Dirichlet-popularity Gumbel-top-K routing; bf16 U[-1,1] tokens, "
+                "N(0,0.02) weights, softmax gates)",
+        "config": {"workload": f"{args.workload} (R={R} virtual ranks, S={S}/rank, E={E}, K={K}, "
+                               f"H={H}, H'={Hp}, B={B}, training)",
+                   "maxvio_targets": list(targets), "global_batch_tokens": R * S,
+                   "l2": "inputs larger than L2 (tens of GB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU, R virtual ranks"},
+        "stages_ms": {s: round(statistics.mean(v), 4) for s, v in stage_ms.items()},
+        "dispatch_combine": {
+            "tokens_per_s": tokens_per_step / ((disp_ms + comb_ms) * 1e-3),
+            "dispatch_gbs": disp_bytes / (disp_ms * 1e-3) / 1e9,
+            "combine_gbs": comb_bytes / (comb_ms * 1e-3) / 1e9,
+            "dispatch_frac_hbm": disp_bytes / (disp_ms * 1e-3) / 1e9 / pk["hbm"],
+            "combine_frac_hbm": comb_bytes / (comb_ms * 1e-3) / 1e9 / pk["hbm"],
+            "frac_vs_8000gbs": (disp_bytes + comb_bytes) / ((disp_ms + comb_ms) * 1e-3) / 1e9 / 8000.0,
+        },
+        "sweep": per_target,
+        "flatness_max_over_min": (max(v["step_ms"] for v in per_target.values()) /
+                                  min(v["step_ms"] for v in per_target.values())) if per_target else None,
+        "roofline": {"kernel": "grouped_gemm", "bound": "tensor", "achieved": gemm_tflops,
+                     "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_sus"],
+                     "peak_source": f"{pk['src']} bf16 sustained (kernel timed inside a long step)",
+                     "traffic": traffic},
+        "e2e": {"value": world * tokens_per_step * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 12 * args.steps,
+        "clocks": clocks,
+    }
+    return result
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_sample(seconds_hint: float = 1.0):
+    """Times the oracle, as it stands, on a bounded sample of the bench workload and
+    scales each stage's cost to one whole step. Runs single-threaded (BLAS threads 1)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+    C = S * K
+    topk = synth.routing(wl, 10.0, 0)
+    t0 = time.perf_counter()
+    p = oracle.plan(topk, E, B, wl.mode)
+    t_plan = time.perf_counter() - t0
+    n = 256                                             # tokens in the data sample
+    x = synth.tokens_host((1, n, H), 1)
+    dest = np.arange(n * K, dtype=np.int32).reshape(1, n, K)
+    g = synth.gates_host(1, n, K, 1)
+    t0 = time.perf_counter()
+    recv = oracle.dispatch(x, dest)
+    t_disp = (time.perf_counter() - t0) * (R * S / n)
+    y = synth.tokens_host((n * K, Hp), 2)
+    t0 = time.perf_counter()
+    oracle.combine(y, dest, g)
+    t_comb = (time.perf_counter() - t0) * (R * S / n)
+    dout = synth.tokens_host((1, n, Hp), 3)
+    t0 = time.perf_counter()
+    oracle.combine_bwd(dout, dest, g)
+    t_bwd = (time.perf_counter() - t0) * (R * S / n)
+    w = synth.weights_host((H, Hp), 4)
+    m = 64                                              # GEMM rows in the sample
+    t0 = time.perf_counter()
+    oracle.gemm_rows(recv[:m], w)
+    t_gemm_rows = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.bf16_to_f32(w).astype(np.float64)
+    t_wconv = time.perf_counter() - t0
+    nseg = int(sum((np.diff(p.cu[u]) > 0).sum() for u in range(R)))
+    t_gemm = (t_gemm_rows - t_wconv) * (R * C / m) + t_wconv * nseg
+    used = int((p.slot_expert >= 0).sum())
+    gsz = (H * Hp) // 16                                # 1/16 of one slot
+    G1 = np.zeros((1, gsz), np.float32)
+    red1 = np.ones((1, 1, gsz), np.float32)
+    t0 = time.perf_counter()
+    oracle.reduce_grad(G1, red1, np.zeros((1, 1), np.int32))
+    t_red = (time.perf_counter() - t0) * 16 * used
+    w_home = synth.weights_host((1, H * Hp // 16), 5)
+    slots = np.zeros((1, 1, H * Hp // 16), np.uint16)
+    t0 = time.perf_counter()
+    oracle.prefetch(w_home, np.zeros((1, 1), np.int32), slots)
+    t_pref = (time.perf_counter() - t0) * 16 * used
+    step_s = t_plan + t_pref + t_disp + t_gemm + t_comb + t_bwd + t_red
+    return {
+        "value": R * S / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "sample": (f"maxvio-10 routing: plan on all {R * S} tokens; dispatch/combine/combine_bwd on "
+                   f"{n} tokens; GEMM on {m} rows + one weight conversion (scaled by {nseg} "
+                   f"segments); prefetch/reduce_grad on 1/16 slot (scaled by {used} slots); "
+                   f"scaled to one step of {R * S} tokens"),
+        "step_seconds_est": step_s,
+        "stages_s": {"plan": t_plan, "prefetch": t_pref, "dispatch": t_disp, "gemm": t_gemm,
+                     "combine": t_comb, "combine_bwd": t_bwd, "reduce_grad": t_red},
+    }
+
+
+def cpu_baseline_subprocess():
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample"], env=env,
+                       capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        res = cpu_baseline_subprocess()
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(res)
+    vals = [r["value"] for r in times if "value" in r]
+    v = statistics.mean(vals) if vals else None
+    base = times[-1] if times else {}
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (8 * 8192 / v * 1e3) if v else None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32/bf16 (oracle)", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} (R=8, S=8192/rank, E=384, K=8, H=7168, H'=2048, B=48)"},
+        "cpu_baseline": {k: base.get(k) for k in ("kind", "cores", "sample")} | {"value": v},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- multi-process
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("BEP_DIST_BACKEND", "gloo")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="bep", choices=("bep", "reference"))
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.cpu_sample:
+        print(json.dumps(cpu_sample()))
+        return
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        return
+    res = run_gpu(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess().items()
+                                   if k in ("value", "unit", "cores", "kind", "sample", "error")}
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * bep.h -- balanced expert-parallel dispatch for one GB300 (sm_103a).
+ *
+ * C ABI of libbep.so. The hot path of MoonEP-style perfectly balanced expert
+ * parallelism: an online planner, a fused permute/dispatch, a grouped expert
+ * GEMM over one [E+B, H, H'] weight tensor addressed by row index, a weighted
+ * combine, and the backward fold (combine backward, reduce_grad).
+ *
+ * Sources (page title / host, then section):
+ *   [P1] "Moonshot AI libera MoonEP ..." (noticiai.com.br)
+ *   [P2] "Moonshot AI Open-Sources MoonEP: A Perfectly Balanced Expert
+ *        Parallelism Library for MoE Training" (spaxe.top)
+ *   [P4] "Moonshot AI open-sources MoonEP" (ai-maestro.online): "The problem
+ *        MoonEP targets", "The core idea: dynamic redundant experts",
+ *        "The memory contract".
+ *
+ * The R ranks are virtual: R partitions of this GPU's HBM. A "remote" write
+ * in the pages is an ordinary global store here.
+ *
+ * Conventions for every call below.
+ *   - Device pointers are caller-owned (the library never frees them), must
+ *     be 16-byte aligned, and must stay valid until the work queued on
+ *     `stream` has finished. Arrays are dense and row-major in the shapes
+ *     given. bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All calls except bep_create/bep_destroy/bep_status are
+ *     asynchronous: nothing synchronises with the host, so a whole step can
+ *     be captured in a CUDA graph.
+ *   - Return value: BEP_OK, or a negative BEP_ERR_* detected on the host
+ *     before anything is queued (the call then has no effect).
+ *   - Errors found on the device (bad expert ids, bounds, a plan that does
+ *     not balance, a timed-out wait) are OR-ed into the context's status
+ *     word; kernels that would read invalid indices skip the bad element.
+ *     bep_status() reads and reports the word.
+ *   - The context owns only its planning/scheduling workspace, allocated
+ *     once in bep_create (static shapes: no allocation afterwards). Calls
+ *     sharing one context must be ordered on one stream.
+ */
+#ifndef BEP_H_
+#define BEP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-side return codes */
+#define BEP_OK          0
+#define BEP_ERR_ARG    -1   /* null pointer, bad dimension or mode value        */
+#define BEP_ERR_ALIGN  -2   /* a pointer is not 16-byte aligned                 */
+#define BEP_ERR_MODE   -3   /* TRAIN needs B == E/R; INFER needs 1 <= B < E/R   */
+#define BEP_ERR_SIZE   -4   /* E % R != 0, R*S*K >= 2^31, or a size limit below */
+#define BEP_ERR_CUDA   -5   /* a CUDA runtime call failed (no device, OOM, ...) */
+
+/* device status word bits (bep_status) */
+#define BEP_DERR_EXPERT_ID   1   /* a top-K id outside [0, E)                     */
+#define BEP_DERR_DUP_ID      2   /* one token names the same expert twice         */
+#define BEP_DERR_INFEASIBLE  4   /* a rank did not end with exactly S*K slots     */
+#define BEP_DERR_BOUNDS      8   /* a dest / cu_seqlens / slot entry out of range */
+#define BEP_DERR_TIMEOUT    16   /* a bounded device wait gave up                 */
+
+/* modes ([P4] "The memory contract": how to set B) */
+#define BEP_TRAIN 0   /* B == E/R: every expert the GEMM touches is local        */
+#define BEP_INFER 1   /* B <  E/R: remote experts beyond B read from home rows   */
+
+/* Size limits checked by bep_create: 1 <= R <= 64, 1 <= E <= 2048, E % R == 0,
+ * 1 <= K <= 32, K <= E, S >= 0, R*S*K < 2^31, H % 64 == 0, H' % 64 == 0,
+ * 64 <= H, 64 <= H'. */
+typedef struct bep_config {
+    int32_t R;     /* virtual ranks                                   */
+    int32_t E;     /* routed experts; home group g owns [g*G, (g+1)*G), G = E/R */
+    int32_t B;     /* prefetch slots per rank                         */
+    int32_t K;     /* top-K experts per token                         */
+    int32_t S;     /* tokens per rank                                 */
+    int32_t H;     /* hidden size (GEMM reduction dim, dispatch row)  */
+    int32_t Hp;    /* H', expert intermediate size (GEMM output dim)  */
+    int32_t mode;  /* BEP_TRAIN or BEP_INFER                          */
+} bep_config;
+
+typedef struct bep_ctx bep_ctx;
+
+/* Validates cfg, selects the current CUDA device, allocates the workspace
+ * (plan tables, GEMM tile table, status word). *out receives the context.
+ * Returns BEP_ERR_ARG/MODE/SIZE for a bad cfg (nothing allocated), or
+ * BEP_ERR_CUDA. */
+int bep_create(const bep_config* cfg, bep_ctx** out);
+
+/* Frees the workspace. Waits for nothing: the caller synchronises first. */
+void bep_destroy(bep_ctx* ctx);
+
+/* The online planner ([P4] "The core idea": redundant experts planned on the
+ * GPU from the current router output so that every rank receives exactly
+ * S*K token-slots; "The problem MoonEP targets": maxvio).
+ *   topk        [R, S, K] int32, expert ids of each token (rank-major tokens)
+ *   cu_seqlens  [R, E+B+1] int32 out: per rank, offsets of the row segments
+ *               0..E+B-1 inside that rank's S*K receive rows; cu[u][0] = 0,
+ *               cu[u][E+B] = S*K. Rows [0,E) are home-expert rows, [E,E+B) are
+ *               the rank's prefetch slots. (The pages' cu_seqlens[E+B] is the
+ *               same data without the leading zero.)
+ *   slot_expert [R, B] int32 out: expert held by each prefetch slot, -1 unused
+ *   dest        [R, S, K] int32 out: flat row index into the [R*S*K] receive
+ *               space for every (token, k); rank u owns rows [u*S*K, (u+1)*S*K)
+ *   maxvio      [1] double out: max_e(T_e / Tbar) - 1, Tbar = R*S*K/E
+ * Deterministic: the same topk always yields the same outputs. */
+int bep_plan(bep_ctx* ctx, const int32_t* topk, int32_t* cu_seqlens, int32_t* slot_expert,
+             int32_t* dest, double* maxvio, void* stream);
+
+/* buffer.prefetch_weight ([P4] "The memory contract": rows [E, E+B) are local
+ * prefetch slots): w_slots[u][j] = w_home[slot_expert[u][j]] for every used
+ * slot; unused slots are left as they are.
+ *   slot_expert [R, B] int32 (from bep_plan)
+ *   w_home      [E, H, H'] bf16, the home rows [0, E)
+ *   w_slots     [R, B, H, H'] bf16, every rank's slots */
+int bep_prefetch_weight(bep_ctx* ctx, const int32_t* slot_expert, const uint16_t* w_home,
+                        uint16_t* w_slots, void* stream);
+
+/* Fused permute/dispatch ([P4] "The core idea", zero copy: tokens are written
+ * directly into their expert-grouped positions): recv[dest[r,t,k], :] = x[r,t,:].
+ *   x    [R, S, H] bf16
+ *   dest [R, S, K] int32 (from bep_plan)
+ *   recv [R*S*K, H] bf16 out, the static per-rank [S*K, H] buffers */
+int bep_dispatch(bep_ctx* ctx, const uint16_t* x, const int32_t* dest, uint16_t* recv,
+                 void* stream);
+
+/* Grouped expert GEMM ([P4] "The memory contract": one [E+B, H, H'] weight
+ * tensor addressed by row index, cu_seqlens selecting the active rows):
+ * for rank u and row rho with a non-empty segment,
+ *   y[u*S*K + seg, :] = recv[u*S*K + seg, :] @ W(u, rho),
+ *   W(u, rho) = rho < E ? w_home[rho] : w_slots[u][rho - E]   ([H, H'] bf16),
+ * bf16 inputs, fp32 accumulation, bf16 (round to nearest even) output.
+ * Rows of y outside every segment are not written. */
+int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                     const uint16_t* w_home, const uint16_t* w_slots, uint16_t* y,
+                     void* stream);
+
+/* Weighted unpermute/combine ([P4] "The core idea": fused permute/unpermute):
+ *   out[r,t,c] = bf16_rne(acc), acc = 0; for k = 0..K-1:
+ *                acc = fmaf(gates[r,t,k], float(y[dest[r,t,k], c]), acc)
+ *   y [R*S*K, D] bf16; dest, gates [R, S, K] (int32, fp32); out [R, S, D] bf16.
+ *   D % 8 == 0 (D = H' after the GEMM). */
+int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const float* gates,
+                int32_t D, uint16_t* out, void* stream);
+
+/* Backward of the combine with respect to y:
+ *   dy[dest[r,t,k], c] = bf16_rne(gates[r,t,k] * float(dout[r,t,c]))  (fp32 product)
+ *   dout [R, S, D] bf16; dy [R*S*K, D] bf16 out. */
+int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest,
+                    const float* gates, int32_t D, uint16_t* dy, void* stream);
+
+/* reduce_grad ([P2]; [P4] "The memory contract": each rank reads its own
+ * experts' slots from every rank's reduce buffer, accumulates them into its
+ * parameter gradient and zeroes the consumed slots):
+ *   for e in [0,E): for r = 0..R-1 ascending: for j with slot_expert[r][j] == e:
+ *       g_home[e] += red[r][j]   (fp32 adds, in this order);   red[r][j] = 0
+ *   slot_expert [R, B] int32; g_home [E, H, H'] fp32 (in/out);
+ *   red [R, B, H, H'] fp32 (in/out: consumed slots become zero). */
+int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, float* red,
+                    void* stream);
+
+/* Waits for `stream`, then reads the status word into *device_err (0 = no
+ * device error). The only call that blocks the host. */
+int bep_status(bep_ctx* ctx, int32_t* device_err, void* stream);
+
+/* Clears the status word (asynchronous, on `stream`). */
+int bep_clear_status(bep_ctx* ctx, void* stream);
+
+/* Static description of a return code or status bit set. */
+const char* bep_strerror(int32_t code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BEP_H_ */

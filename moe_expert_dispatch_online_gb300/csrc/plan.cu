@@ -1,0 +1,488 @@
+// Online planner for balanced expert-parallel dispatch (sm_103a).
+//
+// MoonEP pages: "The core idea: dynamic redundant experts" (ai-maestro.online):
+// a small number of redundant experts is planned on the GPU from the current
+// router output so that every rank receives exactly S*K token-slots; "The
+// problem MoonEP targets": maxvio = max_e(T_e/Tbar) - 1; "The memory contract":
+// training duplicates experts from at most one remote home group per rank
+// (B = E/R), inference (B < E/R) reads overflow experts from their home rows.
+//
+// The planning rule (the pages call the planner "near-optimal" and give no
+// algorithm; this is the library's deterministic choice):
+//   x_g = L_g - C for every home group g (L_g = tokens routed to g's experts).
+//   Donors (x > 0) by x descending, recipients (x < 0) in a deque by deficit
+//   descending, ties by lower g. Pop a recipient, attach it to the current
+//   donor; a donor that overshoots re-enters at the front of the deque with
+//   its new deficit and the next donor takes over.
+//   Group g's slots are listed expert-major, then by (rank, token): g keeps
+//   the first C - inflow_g, each child takes the next `flow` in assignment
+//   order. A replica of expert e on child u sits in slot e - parent(u)*G
+//   (training) or, for inference, in one of B slots given to u's B most-loaded
+//   remote experts (ties: lower id; slots in ascending id) with the rest
+//   overflowing onto home row e.
+//   Each rank's segments follow ascending row order, tokens in (rank, token)
+//   order inside a segment.
+//
+// Kernels, all on one stream, no host synchronisation:
+//   plan_hist  : one CTA per 256-token chunk: validates ids, counts experts per
+//                chunk in shared memory                          -> off[E][NC]
+//   plan_scan  : one CTA per expert: exclusive scan over chunks    -> off, T[E]
+//   plan_solve : one CTA: maxvio, group loads, the tree, expert pieces, slot
+//                map, segment lengths, cu_seqlens, piece bases
+//   plan_dest  : one CTA per chunk: rank of every (token,k) among same-expert
+//                entries (warp __match_any_sync + per-warp shared counters),
+//                then dest = piece base + position in the expert's list.
+
+#include <math.h>
+
+#include "bep_internal.cuh"
+
+namespace bep {
+namespace {
+
+constexpr int kHistThreads = 256;
+constexpr int kScanThreads = 256;
+constexpr int kSolveThreads = 1024;
+constexpr int kDestWarps = kChunkTokens / 32;   // 8 warps, 32 tokens each
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Exclusive scan of one value per thread across the block; returns the
+// exclusive prefix and writes the block total to *total. s_warp: >= 32 ints.
+__device__ int block_excl_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    int incl = warp_incl_scan(v, lane);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? s_warp[lane] : 0;
+        int wi = warp_incl_scan(w, lane);
+        if (lane < nwarps) s_warp[lane] = wi - w;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    int out = s_warp[warp] + incl - v;
+    *total = s_warp[32];
+    __syncthreads();
+    return out;
+}
+
+// In-place exclusive scan of a shared array of n ints; returns the total.
+__device__ int block_excl_scan_array(int* a, int n, int* s_warp) {
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += a[i];
+    int total;
+    int run = block_excl_scan(sum, s_warp, &total);
+    for (int i = lo; i < hi; ++i) {
+        int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kHistThreads) plan_hist_kernel(Dims d, const int32_t* __restrict__ topk,
+                                                                 Workspace ws) {
+    extern __shared__ int32_t s_cnt[];   // [E]
+    const int c = blockIdx.x;
+    const int r = c / d.NCH;
+    const int t0 = (c % d.NCH) * kChunkTokens;
+    const int ntok = min(kChunkTokens, d.S - t0);
+    for (int e = threadIdx.x; e < d.E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    if ((int)threadIdx.x < ntok) {
+        const int32_t* ids = topk + ((int64_t)r * d.S + t0 + threadIdx.x) * d.K;
+        for (int k = 0; k < d.K; ++k) {
+            const int v = ids[k];
+            if (v < 0 || v >= d.E) {
+                bad |= BEP_DERR_EXPERT_ID;
+                continue;
+            }
+            for (int k2 = 0; k2 < k; ++k2)
+                if (ids[k2] == v) bad |= BEP_DERR_DUP_ID;
+            atomicAdd(&s_cnt[v], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < d.E; e += blockDim.x) ws.off[(int64_t)e * d.NC + c] = s_cnt[e];
+    if (bad) {
+        set_status(ws.status, bad);
+        set_status(ws.plan_err, bad);
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(Dims d, Workspace ws) {
+    __shared__ int s_warp[33];
+    const int e = blockIdx.x;
+    int32_t* row = ws.off + (int64_t)e * d.NC;
+    const int per = (d.NC + blockDim.x - 1) / blockDim.x;
+    const int lo = min(d.NC, (int)threadIdx.x * per), hi = min(d.NC, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += row[i];
+    int total;
+    int run = block_excl_scan(sum, s_warp, &total);
+    for (int i = lo; i < hi; ++i) {
+        int v = row[i];
+        row[i] = run;
+        run += v;
+    }
+    if (threadIdx.x == 0) ws.T[e] = total;
+}
+
+__global__ void __launch_bounds__(kSolveThreads) plan_solve_kernel(Dims d, Workspace ws,
+                                                                   int32_t* __restrict__ cu,
+                                                                   int32_t* __restrict__ slot_expert,
+                                                                   double* __restrict__ maxvio) {
+    extern __shared__ int32_t sm[];
+    int32_t* sT = sm;              // [E]
+    int32_t* sGS = sT + d.E;       // [E]  start of expert e inside its group's list
+    int32_t* sNP = sGS + d.E;      // [E+1] piece counts, then first piece
+    __shared__ int s_warp[33];
+    __shared__ int64_t sL[kMaxR];
+    __shared__ int sParent[kMaxR];
+    __shared__ int64_t sInflow[kMaxR];
+    __shared__ int sEdgeDonor[kMaxR], sEdgeChild[kMaxR];
+    __shared__ int64_t sEdgeFlow[kMaxR];
+    __shared__ int sRangeFirst[kMaxR + 1];
+    __shared__ int64_t sRangeEnd[2 * kMaxR];
+    __shared__ int sRangeOwner[2 * kMaxR];
+    __shared__ int sMax, sFail;
+
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int R = d.R, E = d.E, B = d.B, G = d.G, NROW = d.NROW;
+    const int64_t C = d.C;
+
+    if (*(volatile int32_t*)ws.plan_err) {
+        // routing rejected by plan_hist: publish an empty plan
+        for (int i = tid; i < R * (NROW + 1); i += nth) cu[i] = 0;
+        for (int i = tid; i < R * B; i += nth) slot_expert[i] = -1;
+        if (tid == 0) *maxvio = nan("");
+        return;
+    }
+
+    // 1. counts, maxvio ([P4] "The problem MoonEP targets")
+    if (tid == 0) {
+        sMax = 0;
+        sFail = 0;
+    }
+    __syncthreads();
+    int mx = 0;
+    for (int e = tid; e < E; e += nth) {
+        const int v = ws.T[e];
+        sT[e] = v;
+        mx = max(mx, v);
+    }
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((tid & 31) == 0) atomicMax(&sMax, mx);
+    for (int i = tid; i < R * NROW; i += nth) ws.lens[i] = 0;
+    for (int i = tid; i < R * B; i += nth) slot_expert[i] = -1;
+    __syncthreads();
+    if (tid == 0) {
+        const int64_t rsk = (int64_t)R * C;
+        *maxvio = rsk ? (double)((int64_t)E * sMax - rsk) / (double)rsk : 0.0;
+    }
+
+    // 2. group loads and each expert's start inside its group's list
+    if (tid < R) {
+        int64_t run = 0;
+        for (int e = tid * G; e < (tid + 1) * G; ++e) {
+            sGS[e] = (int32_t)run;
+            run += sT[e];
+        }
+        sL[tid] = run;
+    }
+    __syncthreads();
+
+    // 3. the tree (serial over R <= 64 ranks) and each group's ranges
+    if (tid == 0) {
+        int64_t x[kMaxR];
+        int donors[kMaxR], rq[kMaxR];
+        int64_t rdef[kMaxR];
+        int nd = 0, nr = 0;
+        for (int g = 0; g < R; ++g) {
+            x[g] = sL[g] - C;
+            sParent[g] = -1;
+            sInflow[g] = 0;
+            if (x[g] > 0) {      // stable insertion by x descending
+                int p = nd++;
+                while (p > 0 && x[donors[p - 1]] < x[g]) {
+                    donors[p] = donors[p - 1];
+                    --p;
+                }
+                donors[p] = g;
+            } else if (x[g] < 0) {  // stable insertion by deficit descending
+                int p = nr++;
+                while (p > 0 && rdef[p - 1] < -x[g]) {
+                    rq[p] = rq[p - 1];
+                    rdef[p] = rdef[p - 1];
+                    --p;
+                }
+                rq[p] = g;
+                rdef[p] = -x[g];
+            }
+        }
+        int head = 0, di = 0, ne = 0;
+        while (head < nr) {
+            const int u = rq[head];
+            const int64_t D = rdef[head];
+            ++head;
+            if (di >= nd) {
+                sFail = 1;
+                break;
+            }
+            const int dn = donors[di];
+            sParent[u] = dn;
+            sInflow[u] = D;
+            sEdgeDonor[ne] = dn;
+            sEdgeChild[ne] = u;
+            sEdgeFlow[ne] = D;
+            ++ne;
+            x[dn] -= D;
+            if (x[dn] < 0) {      // overshoot: dn now lacks -x, served next
+                --head;
+                rq[head] = dn;
+                rdef[head] = -x[dn];
+                ++di;
+            } else if (x[dn] == 0) {
+                ++di;
+            }
+        }
+        int idx = 0;
+        for (int g = 0; g < R; ++g) {
+            sRangeFirst[g] = idx;
+            int64_t pos = C - sInflow[g];
+            sRangeEnd[idx] = pos;
+            sRangeOwner[idx] = g;
+            ++idx;
+            for (int i = 0; i < ne; ++i)
+                if (sEdgeDonor[i] == g) {
+                    pos += sEdgeFlow[i];
+                    sRangeEnd[idx] = pos;
+                    sRangeOwner[idx] = sEdgeChild[i];
+                    ++idx;
+                }
+            if (pos != sL[g]) sFail = 1;
+        }
+        sRangeFirst[R] = idx;
+    }
+    __syncthreads();
+
+    // 4. pieces: the intersection of each expert's run with its group's ranges
+    for (int e = tid; e < E; e += nth) {
+        const int g = e / G;
+        const int64_t a = sGS[e], b = a + sT[e];
+        int n = 0;
+        int64_t lo = 0;
+        for (int i = sRangeFirst[g]; i < sRangeFirst[g + 1]; ++i) {
+            const int64_t hi = sRangeEnd[i];
+            if (i64max(a, lo) < i64min(b, hi)) ++n;
+            lo = hi;
+        }
+        sNP[e] = n;
+    }
+    __syncthreads();
+    const int npieces = block_excl_scan_array(sNP, E, s_warp);
+    if (tid == 0) sNP[E] = npieces;
+    __syncthreads();
+    for (int e = tid; e < E; e += nth) {
+        const int g = e / G;
+        const int64_t a = sGS[e], b = a + sT[e];
+        int idx = sNP[e];
+        int64_t lo = 0;
+        for (int i = sRangeFirst[g]; i < sRangeFirst[g + 1]; ++i) {
+            const int64_t hi = sRangeEnd[i];
+            const int64_t s0 = i64max(a, lo), s1 = i64min(b, hi);
+            if (s0 < s1) {
+                const int owner = sRangeOwner[i];
+                ws.pstart[idx] = (int32_t)(s0 - a);
+                ws.plen[idx] = (int32_t)(s1 - s0);
+                ws.prank[idx] = owner;
+                int row;
+                if (owner == g) row = e;                                    // home row
+                else if (d.mode == BEP_TRAIN) row = E + (e - g * G);        // slot of the donor group
+                else row = -1;                                              // decided in step 5
+                ws.prow[idx] = row;
+                if (owner != g && d.mode == BEP_TRAIN) slot_expert[owner * B + (e - g * G)] = e;
+                ++idx;
+            }
+            lo = hi;
+        }
+        ws.pfirst[e] = sNP[e];
+    }
+    if (tid == 0) ws.pfirst[E] = npieces;
+    __syncthreads();
+
+    // 5. inference: top-B remote experts of each child get slots, the rest overflow
+    if (d.mode == BEP_INFER) {
+        for (int u = tid; u < R; u += nth) {
+            const int g = sParent[u];
+            if (g < 0) continue;
+            // u's pieces are those of group g's experts with prank == u; their count is plen
+            for (int j = 0; j < B; ++j) {
+                int best = -1, bestlen = -1, bestidx = -1;
+                for (int e = g * G; e < (g + 1) * G; ++e)
+                    for (int i = ws.pfirst[e]; i < ws.pfirst[e + 1]; ++i)
+                        if (ws.prank[i] == u && ws.prow[i] == -1 && ws.plen[i] > bestlen) {
+                            best = e;
+                            bestlen = ws.plen[i];
+                            bestidx = i;
+                        }
+                if (best < 0) break;
+                ws.prow[bestidx] = -2;   // selected
+            }
+            int j = 0;
+            for (int e = g * G; e < (g + 1) * G; ++e)
+                for (int i = ws.pfirst[e]; i < ws.pfirst[e + 1]; ++i)
+                    if (ws.prank[i] == u) {
+                        if (ws.prow[i] == -2) {
+                            ws.prow[i] = E + j;
+                            slot_expert[u * B + j] = e;
+                            ++j;
+                        } else {
+                            ws.prow[i] = e;   // overflow: the GEMM reads home row e
+                        }
+                    }
+        }
+        __syncthreads();
+    }
+
+    // 6. segment lengths (at most one piece per (rank, row)), cu_seqlens per rank
+    for (int i = tid; i < npieces; i += nth) ws.lens[ws.prank[i] * NROW + ws.prow[i]] = ws.plen[i];
+    __syncthreads();
+    {
+        const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+        for (int u = warp; u < R; u += nwarps) {
+            int run = 0;
+            for (int base = 0; base < NROW; base += 32) {
+                const int rr = base + lane;
+                const int v = rr < NROW ? ws.lens[u * NROW + rr] : 0;
+                const int incl = warp_incl_scan(v, lane);
+                if (rr < NROW) cu[u * (NROW + 1) + rr] = run + incl - v;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                cu[u * (NROW + 1) + NROW] = run;
+                if (run != C) sFail = 1;
+            }
+        }
+    }
+    __syncthreads();
+    // 7. dest base of every piece
+    for (int i = tid; i < npieces; i += nth) {
+        const int u = ws.prank[i];
+        ws.pbase[i] = (int32_t)(u * C + cu[u * (NROW + 1) + ws.prow[i]] - ws.pstart[i]);
+    }
+    if (tid == 0 && sFail) {
+        set_status(ws.status, BEP_DERR_INFEASIBLE);
+        set_status(ws.plan_err, BEP_DERR_INFEASIBLE);
+    }
+}
+
+__global__ void __launch_bounds__(kDestWarps * 32) plan_dest_kernel(Dims d, Workspace ws,
+                                                                     const int32_t* __restrict__ topk,
+                                                                     int32_t* __restrict__ dest) {
+    extern __shared__ int32_t sm[];
+    int32_t* s_cnt = sm;                            // [8][E] per-warp counts, then warp bases
+    int32_t* s_lr = sm + kDestWarps * d.E;          // [256*K] rank inside the warp's entries
+    const int c = blockIdx.x;
+    const int r = c / d.NCH;
+    const int t0 = (c % d.NCH) * kChunkTokens;
+    const int ntok = min(kChunkTokens, d.S - t0);
+    const int64_t tok0 = (int64_t)r * d.S + t0;
+    const int K = d.K, E = d.E;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    if (*(volatile int32_t*)ws.plan_err) {
+        for (int q = threadIdx.x; q < ntok * K; q += blockDim.x) dest[tok0 * K + q] = -1;
+        return;
+    }
+    for (int i = threadIdx.x; i < kDestWarps * E; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+
+    // phase 1: each warp ranks its 32 tokens' entries in (token, k) order
+    const int wtok = max(0, min(32, ntok - warp * 32));
+    const int n_ent = wtok * K;
+    const int32_t* wids = topk + (tok0 + warp * 32) * K;
+    int32_t* wcnt = s_cnt + warp * E;
+    int32_t* wlr = s_lr + warp * 32 * K;
+    for (int base = 0; base < 32 * K; base += 32) {
+        const int q = base + lane;
+        const bool valid = q < n_ent;
+        const int e = valid ? wids[q] : -1;
+        const unsigned mask = __match_any_sync(0xffffffffu, e);
+        const int lr = __popc(mask & ((1u << lane) - 1u));
+        int prev = 0;
+        if (valid) {
+            prev = wcnt[e];
+            wlr[q] = prev + lr;
+        }
+        __syncwarp();
+        if (valid && lr == 0) wcnt[e] = prev + __popc(mask);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // phase 2: warp bases = chunk offset + counts of the earlier warps
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = ws.off[(int64_t)e * d.NC + c];
+        for (int w = 0; w < kDestWarps; ++w) {
+            const int v = s_cnt[w * E + e];
+            s_cnt[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+
+    // phase 3: position in the expert's list -> piece -> dest
+    for (int q = lane; q < n_ent; q += 32) {
+        const int e = wids[q];
+        const int p = wcnt[e] + wlr[q];
+        int i = ws.pfirst[e];
+        const int iend = ws.pfirst[e + 1];
+        while (i + 1 < iend && p >= ws.pstart[i] + ws.plen[i]) ++i;
+        dest[(tok0 + warp * 32) * K + q] = ws.pbase[i] + p;
+    }
+}
+
+}  // namespace
+
+cudaError_t plan_setup(int device) {
+    (void)device;
+    cudaError_t err;
+    err = cudaFuncSetAttribute(plan_dest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (kDestWarps * kMaxE + kChunkTokens * kMaxK) * 4);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(plan_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (3 * kMaxE + 1) * 4);
+    return err;
+}
+
+cudaError_t launch_plan(const Dims& d, const Workspace& ws, const int32_t* topk, int32_t* cu,
+                        int32_t* slot_expert, int32_t* dest, double* maxvio, cudaStream_t st) {
+    cudaError_t err = cudaMemsetAsync(ws.plan_err, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+    if (d.NC > 0) {
+        plan_hist_kernel<<<d.NC, kHistThreads, d.E * 4, st>>>(d, topk, ws);
+    }
+    plan_scan_kernel<<<d.E, kScanThreads, 0, st>>>(d, ws);
+    plan_solve_kernel<<<1, kSolveThreads, (3 * d.E + 1) * 4, st>>>(d, ws, cu, slot_expert, maxvio);
+    if (d.NC > 0) {
+        plan_dest_kernel<<<d.NC, kDestWarps * 32, (kDestWarps * d.E + kChunkTokens * d.K) * 4, st>>>(
+            d, ws, topk, dest);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bep

@@ -72,6 +72,7 @@ def _load():
             sig = {
                 "oracle_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
                 "oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+                "oracle_f32_to_bf16_array": (None, [f32p, c64, u16p]),
                 "oracle_histogram": (ci, [i32p, ci, ci, ci, ci, i64p]),
                 "oracle_maxvio": (ctypes.c_double, [i64p, ci, c64]),
                 "oracle_tree": (ci, [ci, i64p, c64, i32p, i64p, i32p]),
@@ -110,6 +111,14 @@ def bf16_to_f32(h: np.ndarray) -> np.ndarray:
 
 def f32_to_bf16_scalar(f: float) -> int:
     return int(_load().oracle_f32_to_bf16(ctypes.c_float(f)))
+
+
+def f32_to_bf16(a: np.ndarray) -> np.ndarray:
+    """float32 array -> bf16 bit patterns, round to nearest even."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_f32_to_bf16_array(_ptr(a, ctypes.c_float), a.size, _ptr(out, ctypes.c_uint16))
+    return out
 
 
 def histogram(topk: np.ndarray, E: int) -> np.ndarray:
@@ -290,3 +299,16 @@ def grouped_gemm(recv: np.ndarray, w_home: np.ndarray, w_slots: np.ndarray, cu: 
             wcache[key] = bf16_to_f32(np.asarray(w)).astype(np.float64)
         y[n] = bf16_to_f32(recv[i]).astype(np.float64) @ wcache[key]
     return y
+
+
+def gemm_rows(a_rows: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y = a @ W in binary64 for bf16 bit-pattern inputs a [n, H], W [H, H']."""
+    A = bf16_to_f32(np.asarray(a_rows)).astype(np.float64)
+    W = bf16_to_f32(np.asarray(w)).astype(np.float64)
+    return A @ W
+
+
+def weight_row_of(rho: int, u: int, E: int, slot_expert: np.ndarray) -> int:
+    """The home expert whose weights serve segment row rho on rank u: rho itself for
+    rho < E, else the expert prefetch_weight copied into slot rho - E."""
+    return int(rho) if rho < E else int(slot_expert[u, rho - E])

@@ -150,6 +150,9 @@ extern "C" {
 
 float oracle_bf16_to_f32(uint16_t h) { return bf16_to_f32(h); }
 uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+void oracle_f32_to_bf16_array(const float* f, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(f[i]);
+}
 
 // T_e = #{(r,t,k) : topk[r,t,k] = e}. Also validates the routing: ids in
 // [0,E) and pairwise distinct within a token (top-K picks K different experts).

@@ -1,0 +1,479 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by
+element on the same seeded inputs. Integer/index/byte outputs bit-exact; combine
+and combine backward bit-exact (fp32 in a fixed k order, one bf16 rounding);
+reduce_grad bit-exact (fixed rank order); the grouped GEMM within 2e-2 relative
+(Frobenius, per segment) of a binary64 product of the bf16 inputs.
+
+At full bench size (R=8, S=8192, E=384, K=8, H=7168, H'=2048) the plan is
+compared in full and the data stages on sampled rows/tokens the oracle computes
+one by one. No oracle input or expected value comes from the CUDA path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+GEMM_RTOL = 2e-2
+_cache = {}
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(DEV).view(
+        torch.bfloat16)
+
+
+def host_u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def routing(name, target, seed):
+    key = ("routing", name, target, seed)
+    if key not in _cache:
+        _cache[key] = synth.routing(synth.WORKLOADS[name], target, seed)
+    return _cache[key]
+
+
+def oracle_plan(name, target, seed):
+    key = ("plan", name, target, seed)
+    if key not in _cache:
+        wl = synth.WORKLOADS[name]
+        _cache[key] = oracle.plan(routing(name, target, seed), wl.E, wl.B, wl.mode)
+    return _cache[key]
+
+
+def cfg_of(bep, wl, **kw):
+    d = dict(R=wl.R, E=wl.E, B=wl.B, K=wl.K, S=wl.S, H=wl.H, Hp=wl.Hp, mode=wl.mode)
+    d.update(kw)
+    return bep.Config(**d)
+
+
+def gpu_plan(bep, cfg, topk):
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, DEV)
+    bep.bep_plan(ctx, torch.from_numpy(np.ascontiguousarray(topk)).to(DEV), buf.cu_seqlens,
+                 buf.slot_expert, buf.dest, buf.maxvio)
+    return ctx, buf
+
+
+def assert_plan_equal(buf, ref):
+    np.testing.assert_array_equal(buf.cu_seqlens.cpu().numpy(), ref.cu)
+    np.testing.assert_array_equal(buf.slot_expert.cpu().numpy(), ref.slot_expert)
+    np.testing.assert_array_equal(buf.dest.cpu().numpy(), ref.dest)
+    assert float(buf.maxvio.item()) == ref.maxvio
+
+
+class Guarded:
+    """A device tensor with 64 KiB canary regions on both sides."""
+    PAD = 65536
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape))
+        esz = torch.empty((), dtype=dtype).element_size()
+        pad = self.PAD // esz
+        self.raw = torch.empty(n + 2 * pad, dtype=dtype, device=DEV)
+        self.raw.view(torch.uint8).fill_(0xA5)
+        self.pad = pad
+        self.t = self.raw[pad:pad + n].view(shape)
+
+    def intact(self):
+        b = self.raw.view(torch.uint8)
+        nb = self.pad * self.raw.element_size()
+        return bool((b[:nb] == 0xA5).all().item() and (b[-nb:] == 0xA5).all().item())
+
+
+# ---------------------------------------------------------------------------- plan
+PLAN_CASES = [("tiny_r2_e8", None, 0)] + \
+    [("train_r8_e64", t, s) for t in (0.2, 1.0, 10.0) for s in (0, 1)] + \
+    [("bench_r8_e384", t, 0) for t in (0.2, 1.0, 10.0, 20.0)] + \
+    [("infer_r8_e384_b4", t, s) for t in (1.0, 20.0) for s in (0, 1)] + \
+    [("grad_r8_e64", 10.0, 0)]
+
+
+@pytest.mark.parametrize("name,target,seed", PLAN_CASES)
+def test_plan_bit_exact(lib, name, target, seed):
+    bep = lib
+    wl = synth.WORKLOADS[name]
+    topk = routing(name, target, seed)
+    ref = oracle_plan(name, target, seed)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert bep.bep_status(ctx) == 0
+    assert_plan_equal(buf, ref)
+    # and it is a valid plan by the rule-independent checker
+    assert oracle.check_plan(topk, wl.E, wl.B, wl.mode, buf.cu_seqlens.cpu().numpy(),
+                             buf.slot_expert.cpu().numpy(), buf.dest.cpu().numpy()) == 0
+
+
+@pytest.mark.parametrize("R,S,K,E,B,mode,how", [
+    (2, 1, 1, 4, 2, 0, "zipf"),          # one token per rank
+    (2, 257, 3, 8, 4, 0, "zipf"),        # ragged chunk tail (256 + 1)
+    (3, 300, 2, 9, 3, 0, "hot"),         # all tokens on the same experts
+    (1, 100, 4, 16, 16, 0, "zipf"),      # a single rank: nothing moves
+    (4, 512, 1, 8, 2, 0, "zipf"),        # K = 1
+    (8, 1024, 4, 64, 8, 0, "roundrobin"),  # perfectly balanced: no replicas
+    (8, 600, 8, 64, 3, 1, "hot"),        # inference, heavy overflow
+    (4, 777, 32, 64, 16, 0, "zipf"),     # K = 32 (the limit)
+    (64, 40, 2, 128, 2, 0, "zipf"),      # R = 64 (the limit)
+])
+def test_plan_edge_cases(lib, R, S, K, E, B, mode, how):
+    bep = lib
+    if how == "zipf":
+        topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 1.2), 7)
+    elif how == "hot":
+        topk = np.broadcast_to(np.arange(K, dtype=np.int32), (R, S, K)).copy()
+    else:
+        topk = synth.round_robin_topk(R, S, K, E)
+    ref = oracle.plan(topk, E, B, mode)
+    cfg = bep.Config(R=R, E=E, B=B, K=K, S=S, H=64, Hp=64, mode=mode)
+    ctx, buf = gpu_plan(bep, cfg, topk)
+    assert bep.bep_status(ctx) == 0
+    assert_plan_equal(buf, ref)
+
+
+def test_plan_empty_batch(lib):
+    bep = lib
+    cfg = bep.Config(R=4, E=16, B=4, K=2, S=0, H=64, Hp=64, mode=0)
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, DEV)
+    topk = torch.zeros((4, 0, 2), dtype=torch.int32, device=DEV)
+    bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio)
+    assert bep.bep_status(ctx) == 0
+    assert not buf.cu_seqlens.any().item()
+    assert (buf.slot_expert == -1).all().item()
+    assert buf.maxvio.item() == 0.0
+
+
+@pytest.mark.parametrize("bad,bit", [("range", 1), ("dup", 2)])
+def test_plan_rejects_bad_routing(lib, bad, bit):
+    bep = lib
+    wl = synth.WORKLOADS["train_r8_e64"]
+    topk = routing("train_r8_e64", 1.0, 0).copy()
+    if bad == "range":
+        topk[3, 17, 2] = wl.E
+    else:
+        topk[5, 900, 1] = topk[5, 900, 0]
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert bep.bep_status(ctx) & bit
+    assert (buf.dest == -1).all().item()
+    assert not buf.cu_seqlens.any().item()
+    # dispatch of an invalid plan writes nothing and reports bounds
+    x = torch.zeros((wl.R, wl.S, wl.H), dtype=torch.bfloat16, device=DEV)
+    g = Guarded((wl.R * wl.C, wl.H), torch.bfloat16)
+    g.t.zero_()
+    bep.bep_dispatch(ctx, x, buf.dest, g.t)
+    assert bep.bep_status(ctx) & bep.BEP_DERR_BOUNDS
+    assert g.intact()
+    # a later valid plan on the same context works (per-call plan error word)
+    bep.bep_clear_status(ctx)
+    good = routing("train_r8_e64", 1.0, 0)
+    bep.bep_plan(ctx, torch.from_numpy(good).to(DEV), buf.cu_seqlens, buf.slot_expert, buf.dest,
+                 buf.maxvio)
+    assert bep.bep_status(ctx) == 0
+    assert_plan_equal(buf, oracle_plan("train_r8_e64", 1.0, 0))
+
+
+# ---------------------------------------------------------------------------- dispatch
+@pytest.mark.parametrize("name,target", [("tiny_r2_e8", None), ("train_r8_e64", 10.0),
+                                         ("grad_r8_e64", 10.0)])
+def test_dispatch_bit_exact(lib, name, target):
+    bep = lib
+    wl = synth.WORKLOADS[name]
+    ref = oracle_plan(name, target, 0)
+    x = synth.tokens_host((wl.R, wl.S, wl.H), 11)
+    recv_ref = oracle.dispatch(x, ref.dest)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing(name, target, 0))
+    g = Guarded((wl.R * wl.C, wl.H), torch.bfloat16)
+    bep.bep_dispatch(ctx, dev_u16(x), buf.dest, g.t)
+    assert bep.bep_status(ctx) == 0
+    assert g.intact()
+    np.testing.assert_array_equal(host_u16(g.t), recv_ref)
+
+
+def _bench_inputs(bep, target):
+    wl = synth.WORKLOADS["bench_r8_e384"]
+    key = ("bench_dev", target)
+    if key not in _cache:
+        _cache.clear()
+        x = synth.tokens_device((wl.R, wl.S, wl.H), 5)
+        _cache[key] = x
+    return wl, _cache[key]
+
+
+@pytest.mark.parametrize("target", [1.0, 20.0])
+def test_dispatch_bench_size_sampled(lib, target):
+    bep = lib
+    wl, x = _bench_inputs(lib, target)
+    topk = synth.routing(wl, target, 0)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert_plan_equal(buf, ref)
+    recv = torch.empty((wl.R * wl.C, wl.H), dtype=torch.bfloat16, device=DEV)
+    recv.view(torch.int16).fill_(-1)
+    bep.bep_dispatch(ctx, x, buf.dest, recv)
+    assert bep.bep_status(ctx) == 0
+    rng = np.random.default_rng(0)
+    flat = rng.choice(wl.R * wl.S * wl.K, size=4096, replace=False)
+    tok = flat // wl.K
+    rows = ref.dest.ravel()[flat]
+    xs = host_u16(x.view(-1, wl.H)[torch.from_numpy(tok).to(DEV)])
+    rs = host_u16(recv[torch.from_numpy(rows.astype(np.int64)).to(DEV)])
+    np.testing.assert_array_equal(rs, xs)
+    # every row of the receive space was written exactly by some token (bijection + full copy):
+    # the sentinel pattern survives nowhere
+    assert not (recv.view(torch.int16) == -1).all(dim=1).any().item()
+    del recv
+
+
+# ---------------------------------------------------------------------------- combine
+@pytest.mark.parametrize("name,target,D", [("tiny_r2_e8", None, 64), ("train_r8_e64", 1.0, 512),
+                                           ("train_r8_e64", 10.0, 1024), ("grad_r8_e64", 10.0, 2048)])
+def test_combine_bit_exact(lib, name, target, D):
+    bep = lib
+    wl = synth.WORKLOADS[name]
+    ref = oracle_plan(name, target, 0)
+    y = synth.tokens_host((wl.R * wl.C, D), 21)
+    gates = synth.gates_host(wl.R, wl.S, wl.K, 3)
+    out_ref = oracle.combine(y, ref.dest, gates)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing(name, target, 0))
+    g = Guarded((wl.R, wl.S, D), torch.bfloat16)
+    bep.bep_combine(ctx, dev_u16(y), buf.dest, torch.from_numpy(gates).to(DEV), g.t)
+    assert bep.bep_status(ctx) == 0
+    assert g.intact()
+    np.testing.assert_array_equal(host_u16(g.t), out_ref)
+
+
+def test_combine_bench_size_sampled(lib):
+    bep = lib
+    wl = synth.WORKLOADS["bench_r8_e384"]
+    topk = synth.routing(wl, 10.0, 0)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    y = synth.tokens_device((wl.R * wl.C, wl.Hp), 31)
+    gates = synth.gates_host(wl.R, wl.S, wl.K, 4)
+    out = torch.empty((wl.R, wl.S, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_combine(ctx, y, buf.dest, torch.from_numpy(gates).to(DEV), out)
+    assert bep.bep_status(ctx) == 0
+    rng = np.random.default_rng(1)
+    toks = rng.choice(wl.R * wl.S, size=2048, replace=False)
+    d = ref.dest.reshape(-1, wl.K)[toks]                     # [n, K] oracle destinations
+    ys = host_u16(y[torch.from_numpy(d.ravel().astype(np.int64)).to(DEV)])   # gathered input rows
+    local = np.arange(len(toks) * wl.K, dtype=np.int32).reshape(1, len(toks), wl.K)
+    g = gates.reshape(-1, wl.K)[toks].reshape(1, len(toks), wl.K)
+    out_ref = oracle.combine(ys, local, g)[0]
+    np.testing.assert_array_equal(host_u16(out.view(-1, wl.Hp)[torch.from_numpy(toks).to(DEV)]),
+                                  out_ref)
+
+
+@pytest.mark.parametrize("name,target,D", [("tiny_r2_e8", None, 128), ("grad_r8_e64", 10.0, 2048)])
+def test_combine_bwd_bit_exact(lib, name, target, D):
+    bep = lib
+    wl = synth.WORKLOADS[name]
+    ref = oracle_plan(name, target, 0)
+    dout = synth.tokens_host((wl.R, wl.S, D), 41)
+    gates = synth.gates_host(wl.R, wl.S, wl.K, 5)
+    dy_ref = oracle.combine_bwd(dout, ref.dest, gates)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing(name, target, 0))
+    g = Guarded((wl.R * wl.C, D), torch.bfloat16)
+    bep.bep_combine_bwd(ctx, dev_u16(dout), buf.dest, torch.from_numpy(gates).to(DEV), g.t)
+    assert bep.bep_status(ctx) == 0
+    assert g.intact()
+    np.testing.assert_array_equal(host_u16(g.t), dy_ref)
+
+
+def test_dispatch_combine_round_trip_identity(lib):
+    """gates = 1/K (K a power of two), combine of the dispatched rows: x again, bit for bit."""
+    bep = lib
+    wl = synth.WORKLOADS["train_r8_e64"]
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing("train_r8_e64", 10.0, 0))
+    x = synth.tokens_device((wl.R, wl.S, wl.H), 9)
+    recv = torch.empty((wl.R * wl.C, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_dispatch(ctx, x, buf.dest, recv)
+    gates = torch.full((wl.R, wl.S, wl.K), 1.0 / wl.K, dtype=torch.float32, device=DEV)
+    out = torch.empty_like(x)
+    bep.bep_combine(ctx, recv, buf.dest, gates, out)
+    assert bep.bep_status(ctx) == 0
+    assert torch.equal(out.view(torch.int16), x.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------- prefetch / reduce_grad
+def test_prefetch_bit_exact(lib):
+    bep = lib
+    wl = synth.WORKLOADS["grad_r8_e64"]
+    ref = oracle_plan("grad_r8_e64", 10.0, 0)
+    w_home = synth.weights_host((wl.E, wl.H, wl.Hp), 2)
+    slots_ref = oracle.prefetch(w_home, ref.slot_expert,
+                                np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.uint16))
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing("grad_r8_e64", 10.0, 0))
+    w_slots = Guarded((wl.R, wl.B, wl.H, wl.Hp), torch.bfloat16)
+    w_slots.t.zero_()
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, dev_u16(w_home), w_slots.t)
+    assert bep.bep_status(ctx) == 0
+    assert w_slots.intact()
+    np.testing.assert_array_equal(host_u16(w_slots.t), slots_ref)
+
+
+def test_reduce_grad_bit_exact(lib):
+    bep = lib
+    wl = synth.WORKLOADS["grad_r8_e64"]
+    ref = oracle_plan("grad_r8_e64", 10.0, 0)
+    assert (ref.slot_expert >= 0).sum() > 0
+    g0 = synth.normal_host((wl.E, wl.H, wl.Hp), 17, 1e-2)
+    red0 = synth.reduce_buffer_host(wl.R, wl.B, wl.H, wl.Hp, ref.slot_expert, 3)
+    g_ref, red_ref = g0.copy(), red0.copy()
+    oracle.reduce_grad(g_ref, red_ref, ref.slot_expert)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing("grad_r8_e64", 10.0, 0))
+    g = torch.from_numpy(g0).to(DEV)
+    red = torch.from_numpy(red0).to(DEV)
+    bep.bep_reduce_grad(ctx, buf.slot_expert, g, red)
+    assert bep.bep_status(ctx) == 0
+    gh = g.cpu().numpy()
+    np.testing.assert_array_equal(gh.view(np.uint32), g_ref.view(np.uint32))
+    assert not red.any().item()
+    rel = np.abs(gh - g_ref).max() / max(np.abs(g_ref).max(), 1e-30)
+    assert rel <= 1e-6
+
+
+# ---------------------------------------------------------------------------- grouped GEMM
+def _gemm_check_full(bep, name, target, seed=0):
+    wl = synth.WORKLOADS[name]
+    ref = oracle_plan(name, target, seed)
+    x = synth.tokens_host((wl.R, wl.S, wl.H), 13)
+    w_home = synth.weights_host((wl.E, wl.H, wl.Hp), 6)
+    recv_ref = oracle.dispatch(x, ref.dest)
+    slots_ref = oracle.prefetch(w_home, ref.slot_expert,
+                                np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.uint16))
+    y_ref = oracle.grouped_gemm(recv_ref, w_home, slots_ref, ref.cu, wl.E)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing(name, target, seed))
+    w_home_d = dev_u16(w_home)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home_d, w_slots)
+    bep.bep_dispatch(ctx, dev_u16(x), buf.dest, buf.recv)
+    g = Guarded((wl.R * wl.C, wl.Hp), torch.bfloat16)
+    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home_d, w_slots, g.t)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    assert g.intact()
+    y = oracle.bf16_to_f32(host_u16(g.t)).astype(np.float64)
+    C = wl.C
+    worst = 0.0
+    for u in range(wl.R):
+        for rho in range(wl.E + wl.B):
+            a, b = ref.cu[u, rho], ref.cu[u, rho + 1]
+            if b == a:
+                continue
+            yr = y_ref[u * C + a:u * C + b]
+            yg = y[u * C + a:u * C + b]
+            err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
+            worst = max(worst, err)
+            assert err <= GEMM_RTOL, (u, rho, err)
+    return worst
+
+
+@pytest.mark.parametrize("name,target", [("tiny_r2_e8", None), ("train_r8_e64", 1.0),
+                                         ("train_r8_e64", 10.0), ("grad_r8_e64", 10.0)])
+def test_grouped_gemm_full(lib, name, target):
+    worst = _gemm_check_full(lib, name, target)
+    print(f"{name} {target}: worst segment rel err {worst:.3e}")
+
+
+@pytest.mark.parametrize("name,target", [("bench_r8_e384", 10.0), ("infer_r8_e384_b4", 20.0)])
+def test_grouped_gemm_bench_size_sampled(lib, name, target):
+    """Full-size GEMM in the bench's launch configuration; the oracle computes sampled
+    rows: first/last row of chosen segments (every rank's first, last and every slot
+    or overflow segment up to a cap) plus random rows, all columns."""
+    bep = lib
+    _cache.clear()
+    torch.cuda.empty_cache()
+    wl = synth.WORKLOADS[name]
+    topk = synth.routing(wl, target, 0)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert_plan_equal(buf, ref)
+    x = synth.tokens_device((wl.R, wl.S, wl.H), 15)
+    w_home = synth.weights_device((wl.E, wl.H, wl.Hp), 8)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots)
+    bep.bep_dispatch(ctx, x, buf.dest, buf.recv)
+    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    # inverse of the oracle's dest: receive row -> token
+    C, E = wl.C, wl.E
+    inv = np.empty(wl.R * C, np.int64)
+    inv[ref.dest.ravel()] = np.arange(wl.R * wl.S * wl.K) // wl.K
+    rng = np.random.default_rng(2)
+    checked = 0
+    for u in range(wl.R):
+        segs = [rho for rho in range(E + wl.B) if ref.cu[u, rho + 1] > ref.cu[u, rho]]
+        remote = [rho for rho in segs if rho >= E or rho // (E // wl.R) != u]
+        pick = sorted(set(segs[:1] + segs[-1:] + remote[:6]))
+        for rho in pick:
+            a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+            rows = sorted(set([a, b - 1] + list(rng.integers(a, b, size=2))))
+            gi = np.array([u * C + r for r in rows], np.int64)
+            a_rows = host_u16(x.view(-1, wl.H)[torch.from_numpy(inv[gi]).to(DEV)])
+            e = oracle.weight_row_of(rho, u, E, ref.slot_expert)
+            w = host_u16(w_home[e])
+            yr = oracle.gemm_rows(a_rows, w)
+            yg = oracle.bf16_to_f32(host_u16(buf.y[torch.from_numpy(gi).to(DEV)])).astype(np.float64)
+            err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
+            assert err <= GEMM_RTOL, (u, rho, err)
+            checked += len(rows)
+    assert checked > 0
+    del w_home, w_slots, x
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------- whole path
+def test_forward_and_backward_fold_in_one_stream_graph(lib):
+    """Capture plan -> prefetch -> dispatch -> GEMM -> combine -> combine_bwd in a
+    CUDA graph (no host synchronisation inside), replay it on new routings, and
+    compare with the oracle."""
+    bep = lib
+    wl = synth.WORKLOADS["train_r8_e64"]
+    cfg = cfg_of(bep, wl)
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, DEV, with_grad=True)
+    topk_d = torch.zeros((wl.R, wl.S, wl.K), dtype=torch.int32, device=DEV)
+    x = dev_u16(synth.tokens_host((wl.R, wl.S, wl.H), 1))
+    w_home_h = synth.weights_host((wl.E, wl.H, wl.Hp), 1)
+    w_home = dev_u16(w_home_h)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    gates_h = synth.gates_host(wl.R, wl.S, wl.K, 1)
+    gates = torch.from_numpy(gates_h).to(DEV)
+    dout_h = synth.tokens_host((wl.R, wl.S, wl.Hp), 2)
+    dout = dev_u16(dout_h)
+    topk_d.copy_(torch.from_numpy(routing("train_r8_e64", 1.0, 0)))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bep.forward(ctx, buf, topk_d, x, gates, w_home, w_slots, stream=s)   # warm-up
+        bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        bep.forward(ctx, buf, topk_d, x, gates, w_home, w_slots, stream=s)
+        bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream=s)
+    for target in (10.0, 0.2):
+        topk = routing("train_r8_e64", target, 1)
+        topk_d.copy_(torch.from_numpy(topk))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle_plan("train_r8_e64", target, 1)
+        assert_plan_equal(buf, ref)
+        x_h = host_u16(x).reshape(wl.R, wl.S, wl.H)
+        recv_ref = oracle.dispatch(x_h, ref.dest)
+        np.testing.assert_array_equal(host_u16(buf.recv), recv_ref)
+        slots_ref = oracle.prefetch(w_home_h, ref.slot_expert,
+                                    np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.uint16))
+        used = ref.slot_expert >= 0
+        np.testing.assert_array_equal(host_u16(w_slots)[used], slots_ref[used])
+        y_ref = oracle.grouped_gemm(recv_ref, w_home_h, slots_ref, ref.cu, wl.E)
+        out_ref = oracle.bf16_to_f32(oracle.combine(oracle.f32_to_bf16(y_ref), ref.dest, gates_h))
+        out = oracle.bf16_to_f32(host_u16(buf.out))
+        assert np.linalg.norm(out - out_ref) / np.linalg.norm(out_ref) <= GEMM_RTOL
+        np.testing.assert_array_equal(host_u16(buf.dy), oracle.combine_bwd(dout_h, ref.dest, gates_h))
+    assert bep.bep_status(ctx) == 0
