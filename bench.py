@@ -173,15 +173,15 @@ def run_gpu(args, rank, world, local_rank):
     if st:
         raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    dist_barrier(world)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
+        time.sleep(1.0)   # nvidia-smi's first sample lands before the work starts
+        for i in range(args.warmup):
+            step(i)
         torch.cuda.synchronize()
+        dist_barrier(world)
         t_start.record(stream)
         for i in range(args.steps):
             step(i, evs[i])
@@ -254,7 +254,7 @@ def run_gpu(args, rank, world, local_rank):
         if not idx:
             continue
         step_ms = [sum(stage_ms[s][i] for s in stages) for i in idx]
-        per_target[f"{t:g}"] = {
+        per_target["zipf1.2" if t is None else f"{t:g}"] = {
             "maxvio": round(maxvios[j], 4), "replicas": nrep[j],
             "step_ms": round(statistics.mean(step_ms), 4),
             **{f"{s}_ms": round(statistics.mean(stage_ms[s][i] for i in idx), 4) for s in stages},
@@ -438,7 +438,7 @@ def dist_max(world, v: float) -> float:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=8)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="bep", choices=("bep", "reference"))
     ap.add_argument("--workload", default=WORKLOAD)

@@ -67,6 +67,9 @@ WORKLOADS = {
     # backward fold: reduce_grad on [E+B, 2048, 1024] fp32 and combine backward
     "grad_r8_e64": Workload("grad_r8_e64", R=8, S=1024, E=64, K=4, H=2048, Hp=1024, B=8,
                             mode=MODE_TRAIN),
+    # the bench's expert shape (H=7168, H'=2048) on a few GB: profiling captures
+    "gemm_probe_r4_e16": Workload("gemm_probe_r4_e16", R=4, S=2048, E=16, K=8, H=7168, Hp=2048,
+                                  B=4, mode=MODE_TRAIN),
 }
 
 MAXVIO_TARGETS = {
@@ -75,6 +78,7 @@ MAXVIO_TARGETS = {
     "bench_r8_e384": (0.2, 1.0, 10.0, 20.0),
     "infer_r8_e384_b4": (1.0, 20.0),
     "grad_r8_e64": (10.0,),
+    "gemm_probe_r4_e16": (None,),
 }
 
 
