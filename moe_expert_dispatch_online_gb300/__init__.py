@@ -35,9 +35,9 @@ BEP_TRAIN = 0
 BEP_INFER = 1
 
 # every entry point declared in include/bep.h
-SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_prefetch_weight", "bep_dispatch",
-           "bep_grouped_gemm", "bep_combine", "bep_combine_bwd", "bep_reduce_grad", "bep_status",
-           "bep_clear_status", "bep_strerror")
+SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_prefetch_weight",
+           "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd", "bep_reduce_grad",
+           "bep_status", "bep_clear_status", "bep_strerror")
 
 _lib = None
 _lock = threading.Lock()
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH):
             "bep_create": (ctypes.c_int, [ctypes.POINTER(_Config), ctypes.POINTER(vp)]),
             "bep_destroy": (None, [vp]),
             "bep_plan": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
+            "bep_plan_noalloc": (ctypes.c_int, [ctypes.POINTER(_Config), p, p, p, p, p, p, vp]),
             "bep_prefetch_weight": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_dispatch": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_grouped_gemm": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
@@ -206,6 +207,28 @@ def bep_plan(ctx: Context, topk, cu_seqlens, slot_expert, dest, maxvio, stream=N
                            _ptr(cu_seqlens, _i32(), "cu_seqlens"),
                            _ptr(slot_expert, _i32(), "slot_expert"), _ptr(dest, _i32(), "dest"),
                            _ptr(maxvio, (torch.float64,), "maxvio"), _stream(stream)), "bep_plan")
+
+
+def bep_plan_noalloc(cfg: Config, topk, cu_seqlens, slot_expert, dest, maxvio, device_err,
+                     stream=None):
+    """bep_plan without a context and without allocating (scratch in a static device
+    array inside the library); device_err receives this call's BEP_DERR_* bits."""
+    import torch
+    c = cfg
+    _numel(topk, c.R * c.S * c.K, "topk")
+    _numel(dest, c.R * c.S * c.K, "dest")
+    _numel(cu_seqlens, c.R * (c.E + c.B + 1), "cu_seqlens")
+    _numel(slot_expert, c.R * c.B, "slot_expert")
+    _numel(maxvio, 1, "maxvio")
+    _numel(device_err, 1, "device_err")
+    cc = _Config(c.R, c.E, c.B, c.K, c.S, c.H, c.Hp, c.mode)
+    _check(load().bep_plan_noalloc(ctypes.byref(cc), _ptr(topk, _i32(), "topk"),
+                                   _ptr(cu_seqlens, _i32(), "cu_seqlens"),
+                                   _ptr(slot_expert, _i32(), "slot_expert"),
+                                   _ptr(dest, _i32(), "dest"),
+                                   _ptr(maxvio, (torch.float64,), "maxvio"),
+                                   _ptr(device_err, _i32(), "device_err"), _stream(stream)),
+           "bep_plan_noalloc")
 
 
 def bep_prefetch_weight(ctx: Context, slot_expert, w_home, w_slots, stream=None):

@@ -14,10 +14,10 @@ struct bep_ctx {
 };
 
 namespace {
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
 
-int make_dims(const bep_config* c, bep::Dims* d) {
+int bep::make_dims(const bep_config* c, bep::Dims* d) {
     if (c->R < 1 || c->E < 1 || c->K < 1 || c->S < 0 || c->B < 0 || c->H < 1 || c->Hp < 1)
         return BEP_ERR_ARG;
     if (c->mode != BEP_TRAIN && c->mode != BEP_INFER) return BEP_ERR_ARG;
@@ -47,6 +47,8 @@ int make_dims(const bep_config* c, bep::Dims* d) {
     return BEP_OK;
 }
 
+namespace {
+
 template <typename T>
 T* carve(char*& p, size_t n) {
     T* out = reinterpret_cast<T*>(p);
@@ -67,7 +69,7 @@ int bep_create(const bep_config* cfg, bep_ctx** out) {
     if (!cfg || !out) return BEP_ERR_ARG;
     *out = nullptr;
     bep::Dims d;
-    int rc = make_dims(cfg, &d);
+    int rc = bep::make_dims(cfg, &d);
     if (rc) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BEP_ERR_CUDA;

@@ -55,6 +55,9 @@ struct Dims {
     int max_tiles;  // GEMM m-tiles upper bound
 };
 
+// configuration checks shared by the entry points (bep.cu)
+int make_dims(const bep_config* c, Dims* d);
+
 // planner (plan.cu)
 cudaError_t plan_setup(int device);
 cudaError_t launch_plan(const Dims& d, const Workspace& ws, const int32_t* topk, int32_t* cu,

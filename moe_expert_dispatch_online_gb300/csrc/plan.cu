@@ -486,3 +486,102 @@ cudaError_t launch_plan(const Dims& d, const Workspace& ws, const int32_t* topk,
 }
 
 }  // namespace bep
+
+// ---------------------------------------------------------------------------
+// Planner entry point that allocates nothing (declared in include/bep.h).
+//
+// Some callers cannot call cudaMalloc when they plan: code that runs while a
+// stream is being captured into a CUDA graph (allocation is not allowed
+// there), services whose memory pool is fixed after warm-up, and embedders
+// that cannot hold a bep_ctx. This variant takes the configuration directly
+// and keeps the planner's scratch tables in a file-scope device array that
+// every GPU loading the library reserves until the process exits.
+//
+// Host code must not hand the array's symbol to a kernel: on the host it is a
+// stand-in, not a device address. The device address is fetched with
+// cudaGetSymbolAddress once per device, on that device's first call, which
+// also sets the planner kernels' shared-memory limits. That first call should
+// therefore come before any stream capture. Every call shares the one array:
+// calls whose work overlaps on the GPU (other streams, other threads) race on
+// it and must be serialised by the caller.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;   // 2 MiB
+constexpr int kNoAllocMaxDevices = 64;
+
+__device__ __align__(256) int32_t g_plan_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
+
+std::mutex g_noalloc_mutex;
+int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Scratch bytes the planner needs for d (the same tables bep_create carves).
+size_t noalloc_bytes(const bep::Dims& d) {
+    const size_t E = d.E, R = d.R, NC = d.NC, NROW = d.NROW, NP = (size_t)d.E + d.R;
+    auto rnd = [](size_t n) { return (n * sizeof(int32_t) + 255) & ~(size_t)255; };
+    return rnd(1) + rnd(E * (NC > 0 ? NC : 1)) + rnd(E) + rnd(R * NROW) + rnd(E + 1) + 5 * rnd(NP);
+}
+
+int32_t* carve_i32(char*& p, size_t n) {
+    int32_t* out = reinterpret_cast<int32_t*>(p);
+    p += (n * sizeof(int32_t) + 255) & ~(size_t)255;
+    return out;
+}
+
+}  // namespace
+
+extern "C" int bep_plan_noalloc(const bep_config* cfg, const int32_t* topk, int32_t* cu_seqlens,
+                                int32_t* slot_expert, int32_t* dest, double* maxvio,
+                                int32_t* device_err, void* stream) {
+    if (!cfg || !cu_seqlens || !maxvio || !device_err) return BEP_ERR_ARG;
+    bep::Dims d;
+    const int rc = bep::make_dims(cfg, &d);
+    if (rc) return rc;
+    if (d.R * d.B > 0 && !slot_expert) return BEP_ERR_ARG;
+    if (d.C > 0 && (!topk || !dest)) return BEP_ERR_ARG;
+    auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
+    if (!al(topk, 4) || !al(cu_seqlens, 4) || !al(slot_expert, 4) || !al(dest, 4) ||
+        !al(maxvio, 8) || !al(device_err, 4))
+        return BEP_ERR_ALIGN;
+    if (noalloc_bytes(d) > kNoAllocScratchBytes) return BEP_ERR_SIZE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BEP_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return BEP_ERR_ARG;
+    int32_t* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_addr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || !p) return BEP_ERR_CUDA;
+            if (bep::plan_setup(dev) != cudaSuccess) return BEP_ERR_CUDA;
+            g_noalloc_addr[dev] = static_cast<int32_t*>(p);
+        }
+        base = g_noalloc_addr[dev];
+    }
+
+    // The planner's tables, carved from the static array in bep_create's order. Only the
+    // per-call error word must start at zero (launch_plan clears it); every other table is
+    // fully rewritten by the kernels before it is read.
+    char* p = reinterpret_cast<char*>(base);
+    bep::Workspace ws = {};
+    ws.status = device_err;
+    ws.plan_err = carve_i32(p, 1);
+    ws.off = carve_i32(p, (size_t)d.E * (d.NC > 0 ? d.NC : 1));
+    ws.T = carve_i32(p, d.E);
+    ws.lens = carve_i32(p, (size_t)d.R * d.NROW);
+    ws.pfirst = carve_i32(p, (size_t)d.E + 1);
+    ws.pstart = carve_i32(p, (size_t)d.E + d.R);
+    ws.plen = carve_i32(p, (size_t)d.E + d.R);
+    ws.prank = carve_i32(p, (size_t)d.E + d.R);
+    ws.prow = carve_i32(p, (size_t)d.E + d.R);
+    ws.pbase = carve_i32(p, (size_t)d.E + d.R);
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(device_err, 0, sizeof(int32_t), st) != cudaSuccess) return BEP_ERR_CUDA;
+    return bep::launch_plan(d, ws, topk, cu_seqlens, slot_expert, dest, maxvio, st) == cudaSuccess
+               ? BEP_OK
+               : BEP_ERR_CUDA;
+}
