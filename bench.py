@@ -195,41 +195,63 @@ def run_gpu(args, rank, world, local_rank):
     if st:
         raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers. Every step uploads its
+    # inputs (topk, x, gates, dOut) from pinned host memory and downloads its output.
+    # Inputs and outputs are double-buffered on the device and the copies run on a
+    # second stream, so step i+2's upload and step i's download overlap compute.
     x_h = x.cpu().pin_memory()
     dout_h = dout.cpu().pin_memory()
     gates_h = gates.cpu().pin_memory()
     topks_h = [t.cpu().pin_memory() for t in topks]
-    out_h = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
-    topk_d = torch.empty_like(topks[0])
+    out_h = [torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory() for _ in range(2)]
+    dbl = [dict(topk=torch.empty_like(topks[0]), x=torch.empty_like(x), g=torch.empty_like(gates),
+                dout=torch.empty_like(dout), out=torch.empty_like(buf.out)) for _ in range(2)]
     h2d = x_h.numel() * 2 + dout_h.numel() * 2 + gates_h.numel() * 4 + topks_h[0].numel() * 4
-    d2h = out_h.numel() * 2
+    d2h = out_h[0].numel() * 2
+    copy_stream = torch.cuda.Stream(device=dev)
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
-        with torch.cuda.stream(stream):
-            topk_d.copy_(topks_h[i % len(topks_h)], non_blocking=True)
-            x.copy_(x_h, non_blocking=True)
-            gates.copy_(gates_h, non_blocking=True)
-            dout.copy_(dout_h, non_blocking=True)
-        bep.bep_plan(ctx, topk_d, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
-        bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
-        bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
-        bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
-        bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
-        bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream)
-        bep.bep_reduce_grad(ctx, buf.slot_expert, g_home, red, stream)
-        with torch.cuda.stream(stream):
-            out_h.copy_(buf.out, non_blocking=True)
+    def upload(i):
+        b = dbl[i % 2]
+        with torch.cuda.stream(copy_stream):
+            b["topk"].copy_(topks_h[i % len(topks_h)], non_blocking=True)
+            b["x"].copy_(x_h, non_blocking=True)
+            b["g"].copy_(gates_h, non_blocking=True)
+            b["dout"].copy_(dout_h, non_blocking=True)
+            loaded[i % 2].record(copy_stream)
 
-    for i in range(min(args.warmup, 3)):
-        e2e_step(i)
+    def e2e_run(n):
+        upload(0)
+        if n > 1:
+            upload(1)
+        for i in range(n):
+            b = dbl[i % 2]
+            stream.wait_event(loaded[i % 2])
+            bep.bep_plan(ctx, b["topk"], buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio,
+                         stream)
+            bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+            bep.bep_dispatch(ctx, b["x"], buf.dest, buf.recv, stream)
+            bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
+            bep.bep_combine(ctx, buf.y, buf.dest, b["g"], b["out"], stream)
+            bep.bep_combine_bwd(ctx, b["dout"], buf.dest, b["g"], buf.dy, stream)
+            bep.bep_reduce_grad(ctx, buf.slot_expert, g_home, red, stream)
+            consumed[i % 2].record(stream)
+            copy_stream.wait_event(consumed[i % 2])
+            with torch.cuda.stream(copy_stream):
+                out_h[i % 2].copy_(b["out"], non_blocking=True)
+            if i + 2 < n:
+                upload(i + 2)
+        stream.wait_stream(copy_stream)
+
+    e2e_run(min(args.warmup, 3))
     torch.cuda.synchronize()
     dist_barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
+    copy_stream.wait_event(e0)
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)

@@ -322,33 +322,55 @@ __global__ void __launch_bounds__(1024) reduce_grad_prep_kernel(const int32_t* _
 }
 
 // g_home[e] += red[slot] for its slots in order (fp32 adds), then the slots are zeroed.
+// Work items are (touched expert, 32 KB tile of its gradient), strided over a
+// persistent grid. Each thread owns kRedU float4 of the tile: it issues all of
+// their gradient loads, then, slot by slot in ascending order, all of that
+// slot's loads, before any add, so kRedU independent 16-byte loads are in
+// flight per operand.
+constexpr int kRedU = 8;
+
 __global__ void __launch_bounds__(kThreads) reduce_grad_kernel(float4* __restrict__ g_home,
                                                                float4* __restrict__ red, int64_t nvec,
                                                                Workspace ws) {
     const int count = *ws.rg_count;
-    const int64_t tile_vec = (int64_t)kThreads * 4;
+    const int64_t tile_vec = (int64_t)kThreads * kRedU;
     const int64_t ntile = (nvec + tile_vec - 1) / tile_vec;
-    for (int it = 0; it < count; ++it) {
+    const int64_t nitems = (int64_t)count * ntile;
+    for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int it = (int)(item / ntile);
+        const int64_t base = (item - (int64_t)it * ntile) * tile_vec + threadIdx.x;
         const int e = ws.rg_expert[it];
         const int s0 = ws.rg_first[it], s1 = ws.rg_first[it + 1];
         float4* g = g_home + (int64_t)e * nvec;
-        for (int64_t t = blockIdx.x; t < ntile; t += gridDim.x) {
+        float4 acc[kRedU];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t i = t * tile_vec + (int64_t)u * kThreads + threadIdx.x;
-                if (i >= nvec) continue;
-                float4 acc = g[i];
-                for (int s = s0; s < s1; ++s) {
-                    float4* r = red + (int64_t)ws.rg_slot[s] * nvec + i;
-                    const float4 v = *r;
-                    acc.x = __fadd_rn(acc.x, v.x);
-                    acc.y = __fadd_rn(acc.y, v.y);
-                    acc.z = __fadd_rn(acc.z, v.z);
-                    acc.w = __fadd_rn(acc.w, v.w);
-                    *r = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                g[i] = acc;
+        for (int u = 0; u < kRedU; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) acc[u] = g[i];
+        }
+        for (int s = s0; s < s1; ++s) {
+            float4* r = red + (int64_t)ws.rg_slot[s] * nvec;
+            float4 v[kRedU];
+#pragma unroll
+            for (int u = 0; u < kRedU; ++u) {
+                const int64_t i = base + (int64_t)u * kThreads;
+                if (i < nvec) v[u] = r[i];
             }
+#pragma unroll
+            for (int u = 0; u < kRedU; ++u) {
+                const int64_t i = base + (int64_t)u * kThreads;
+                if (i >= nvec) continue;
+                acc[u].x = __fadd_rn(acc[u].x, v[u].x);
+                acc[u].y = __fadd_rn(acc[u].y, v[u].y);
+                acc[u].z = __fadd_rn(acc[u].z, v[u].z);
+                acc[u].w = __fadd_rn(acc[u].w, v[u].w);
+                r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRedU; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) g[i] = acc[u];
         }
     }
 }
@@ -413,7 +435,7 @@ cudaError_t launch_reduce_grad(const Dims& d, const Workspace& ws, const int32_t
     if (nslots == 0) return cudaSuccess;
     reduce_grad_prep_kernel<<<1, 1024, (nslots + 2 * d.E) * 4, st>>>(slot_expert, nslots, d.E, ws);
     const int64_t nvec = (int64_t)d.H * d.Hp / 4;
-    reduce_grad_kernel<<<num_sms * kCtasPerSm / 2, kThreads, 0, st>>>(
+    reduce_grad_kernel<<<num_sms * 4, kThreads, 0, st>>>(
         reinterpret_cast<float4*>(g_home), reinterpret_cast<float4*>(red), nvec, ws);
     return cudaGetLastError();
 }
