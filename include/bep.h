@@ -170,6 +170,40 @@ int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const floa
 int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest,
                     const float* gates, int32_t D, uint16_t* dy, void* stream);
 
+/* Backward of the dispatch ([P4] "The core idea": in the backward pass the
+ * gradients flow back to where the tokens came from): every token's gradient
+ * is the sum of the gradients of its K receive rows,
+ *   dx[r,t,c] = bf16_rne(acc), acc = 0; for k = 0..K-1: acc = acc + float(drecv[dest[r,t,k], c])
+ *   drecv [R*S*K, H] bf16; dest [R, S, K] int32; dx [R, S, H] bf16 out. */
+int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, uint16_t* dx,
+                     void* stream);
+
+/* Input gradient of the grouped expert GEMM ([P4] "The memory contract": the
+ * same [E+B, H, H'] rows serve the backward pass): for rank u and every
+ * non-empty segment rho,
+ *   drecv[u*S*K + seg, :] = dy[u*S*K + seg, :] @ W(u, rho)^T,
+ * W(u, rho) as in bep_grouped_gemm; bf16 in, fp32 accumulate, bf16 out.
+ *   dy [R*S*K, H'] bf16; drecv [R*S*K, H] bf16 out (rows outside every segment
+ *   are not written). */
+int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* dy,
+                        const uint16_t* w_home, const uint16_t* w_slots, uint16_t* drecv,
+                        void* stream);
+
+/* Weight gradient of the grouped expert GEMM ([P2]; [P4] "The memory contract":
+ * training mirrors the weight layout in an fp32 [E+B, H, H'] gradient whose
+ * rows [E, E+B) are a separate reduce buffer, invisible to the framework's own
+ * gradient reduce): for rank u and every non-empty segment rho,
+ *   rho <  E: g_home[rho]            += recv[seg]^T @ dy[seg]
+ *   rho >= E: red[u][rho - E]        += recv[seg]^T @ dy[seg]
+ * bf16 in, fp32 accumulate; the fp32 products are added to the existing
+ * contents (one fp32 add per element). Training mode only (BEP_ERR_MODE
+ * otherwise: with overflow rows two segments would share a home row);
+ * H % 128 == 0 (BEP_ERR_SIZE otherwise).
+ *   recv [R*S*K, H] bf16; dy [R*S*K, H'] bf16; g_home [E, H, H'] fp32 in/out;
+ *   red [R, B, H, H'] fp32 in/out. */
+int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                        const uint16_t* dy, float* g_home, float* red, void* stream);
+
 /* reduce_grad ([P2]; [P4] "The memory contract": each rank reads its own
  * experts' slots from every rank's reduce buffer, accumulates them into its
  * parameter gradient and zeroes the consumed slots):

@@ -36,7 +36,8 @@ BEP_INFER = 1
 
 # every entry point declared in include/bep.h
 SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_prefetch_weight",
-           "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd", "bep_reduce_grad",
+           "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd",
+           "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw", "bep_reduce_grad",
            "bep_status", "bep_clear_status", "bep_strerror")
 
 _lib = None
@@ -73,6 +74,9 @@ def load(path: str = LIB_PATH):
             "bep_grouped_gemm": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_combine": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
             "bep_combine_bwd": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
+            "bep_dispatch_bwd": (ctypes.c_int, [vp, p, p, p, vp]),
+            "bep_grouped_gemm_dx": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
+            "bep_grouped_gemm_dw": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_reduce_grad": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_status": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "bep_clear_status": (ctypes.c_int, [vp, vp]),
@@ -286,6 +290,43 @@ def bep_combine_bwd(ctx: Context, dout, dest, gates, dy, stream=None):
     _check(load().bep_combine_bwd(ctx.handle, _ptr(dout, _bf16(), "dout"),
                                   _ptr(dest, _i32(), "dest"), _ptr(gates, _f32(), "gates"), D,
                                   _ptr(dy, _bf16(), "dy"), _stream(stream)), "bep_combine_bwd")
+
+
+def bep_dispatch_bwd(ctx: Context, drecv, dest, dx, stream=None):
+    c = ctx.cfg
+    _numel(drecv, c.R * c.C * c.H, "drecv")
+    _numel(dest, c.R * c.S * c.K, "dest")
+    _numel(dx, c.R * c.S * c.H, "dx")
+    _check(load().bep_dispatch_bwd(ctx.handle, _ptr(drecv, _bf16(), "drecv"),
+                                   _ptr(dest, _i32(), "dest"), _ptr(dx, _bf16(), "dx"),
+                                   _stream(stream)), "bep_dispatch_bwd")
+
+
+def bep_grouped_gemm_dx(ctx: Context, cu_seqlens, dy, w_home, w_slots, drecv, stream=None):
+    c = ctx.cfg
+    _numel(cu_seqlens, c.R * (c.E + c.B + 1), "cu_seqlens")
+    _numel(dy, c.R * c.C * c.Hp, "dy")
+    _numel(w_home, c.E * c.H * c.Hp, "w_home")
+    _numel(w_slots, c.R * c.B * c.H * c.Hp, "w_slots")
+    _numel(drecv, c.R * c.C * c.H, "drecv")
+    _check(load().bep_grouped_gemm_dx(ctx.handle, _ptr(cu_seqlens, _i32(), "cu_seqlens"),
+                                      _ptr(dy, _bf16(), "dy"), _ptr(w_home, _bf16(), "w_home"),
+                                      _ptr(w_slots, _bf16(), "w_slots"),
+                                      _ptr(drecv, _bf16(), "drecv"), _stream(stream)),
+           "bep_grouped_gemm_dx")
+
+
+def bep_grouped_gemm_dw(ctx: Context, cu_seqlens, recv, dy, g_home, red, stream=None):
+    c = ctx.cfg
+    _numel(cu_seqlens, c.R * (c.E + c.B + 1), "cu_seqlens")
+    _numel(recv, c.R * c.C * c.H, "recv")
+    _numel(dy, c.R * c.C * c.Hp, "dy")
+    _numel(g_home, c.E * c.H * c.Hp, "g_home")
+    _numel(red, c.R * c.B * c.H * c.Hp, "red")
+    _check(load().bep_grouped_gemm_dw(ctx.handle, _ptr(cu_seqlens, _i32(), "cu_seqlens"),
+                                      _ptr(recv, _bf16(), "recv"), _ptr(dy, _bf16(), "dy"),
+                                      _ptr(g_home, _f32(), "g_home"), _ptr(red, _f32(), "red"),
+                                      _stream(stream)), "bep_grouped_gemm_dw")
 
 
 def bep_reduce_grad(ctx: Context, slot_expert, g_home, red, stream=None):

@@ -210,6 +210,44 @@ int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest, con
                                            ctx->num_sms, as_stream(stream)));
 }
 
+int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, uint16_t* dx,
+                     void* stream) {
+    if (!ctx) return BEP_ERR_ARG;
+    if (ctx->d.C == 0) return BEP_OK;
+    if (!drecv || !dest || !dx) return BEP_ERR_ARG;
+    if (!aligned(drecv, 16) || !aligned(dx, 16) || !aligned(dest, 4)) return BEP_ERR_ALIGN;
+    return cuda_rc(bep::launch_dispatch_bwd(ctx->d, ctx->ws, drecv, dest, dx, ctx->num_sms,
+                                            as_stream(stream)));
+}
+
+int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* dy,
+                        const uint16_t* w_home, const uint16_t* w_slots, uint16_t* drecv,
+                        void* stream) {
+    if (!ctx) return BEP_ERR_ARG;
+    if (ctx->d.C == 0) return BEP_OK;
+    if (!cu_seqlens || !dy || !w_home || !drecv) return BEP_ERR_ARG;
+    if (ctx->d.R * ctx->d.B > 0 && !w_slots) return BEP_ERR_ARG;
+    if (!aligned(cu_seqlens, 4) || !aligned(dy, 16) || !aligned(w_home, 16) ||
+        !aligned(w_slots, 16) || !aligned(drecv, 16))
+        return BEP_ERR_ALIGN;
+    return cuda_rc(bep::launch_grouped_gemm_dx(ctx->d, ctx->ws, cu_seqlens, dy, w_home, w_slots,
+                                               drecv, ctx->num_sms, as_stream(stream)));
+}
+
+int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                        const uint16_t* dy, float* g_home, float* red, void* stream) {
+    if (!ctx) return BEP_ERR_ARG;
+    if (ctx->d.mode != BEP_TRAIN) return BEP_ERR_MODE;
+    if (ctx->d.H % bep::kBM != 0) return BEP_ERR_SIZE;
+    if (ctx->d.C == 0) return BEP_OK;
+    if (!cu_seqlens || !recv || !dy || !g_home || !red) return BEP_ERR_ARG;
+    if (!aligned(cu_seqlens, 4) || !aligned(recv, 16) || !aligned(dy, 16) ||
+        !aligned(g_home, 16) || !aligned(red, 16))
+        return BEP_ERR_ALIGN;
+    return cuda_rc(bep::launch_grouped_gemm_dw(ctx->d, ctx->ws, cu_seqlens, recv, dy, g_home, red,
+                                               ctx->num_sms, as_stream(stream)));
+}
+
 int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, float* red,
                     void* stream) {
     if (!ctx) return BEP_ERR_ARG;

@@ -74,6 +74,8 @@ cudaError_t launch_combine(const Dims& d, const Workspace& ws, const uint16_t* y
 cudaError_t launch_combine_bwd(const Dims& d, const Workspace& ws, const uint16_t* dout,
                                const int32_t* dest, const float* gates, int D, uint16_t* dy,
                                int num_sms, cudaStream_t st);
+cudaError_t launch_dispatch_bwd(const Dims& d, const Workspace& ws, const uint16_t* drecv,
+                                const int32_t* dest, uint16_t* dx, int num_sms, cudaStream_t st);
 cudaError_t launch_reduce_grad(const Dims& d, const Workspace& ws, const int32_t* slot_expert,
                                float* g_home, float* red, int num_sms, cudaStream_t st);
 // grouped GEMM (gemm.cu)
@@ -82,6 +84,13 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
                                 const uint16_t* recv, const uint16_t* w_home,
                                 const uint16_t* w_slots, uint16_t* y, int num_sms,
                                 cudaStream_t st);
+cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* dy, const uint16_t* w_home,
+                                   const uint16_t* w_slots, uint16_t* drecv, int num_sms,
+                                   cudaStream_t st);
+cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* recv, const uint16_t* dy, float* g_home,
+                                   float* red, int num_sms, cudaStream_t st);
 
 __device__ __forceinline__ int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }

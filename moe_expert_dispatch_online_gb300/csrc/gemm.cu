@@ -1,27 +1,36 @@
-// Grouped expert GEMM over one [E+B, H, H'] weight tensor (sm_103a, tcgen05).
+// Grouped expert GEMMs over one [E+B, H, H'] weight tensor (sm_103a, tcgen05).
 //
 // MoonEP pages (ai-maestro.online), "The memory contract": the group GEMM
 // consumes a single [E+B, H, H'] weight tensor and addresses experts purely by
 // row index; cu_seqlens from the planner selects the active rows. Rows [0, E)
 // are the home experts, rows [E, E+B) a rank's prefetch slots; overflow
-// experts (inference) are read from their home rows.
+// experts (inference) are read from their home rows. In training the fp32
+// gradient mirrors the layout: rows [0, E) are the parameter gradient, rows
+// [E, E+B) a separate reduce buffer that reduce_grad folds back.
+//
+// Three products share one kernel (template MODE):
+//   FWD  Y[seg]     = recv[seg] @ W(u,rho)          A: recv, K-major  B: W, MN-major
+//   DX   dRecv[seg] = dY[seg] @ W(u,rho)^T          A: dY, K-major    B: W^T, K-major
+//   DW   dW(u,rho) += recv[seg]^T @ dY[seg] (fp32)  A: recv^T, MN-major  B: dY, MN-major
+//        dW of a home row accumulates into g_home[rho], of slot j into red[u][j].
 //
 // Design (one GB300):
-//   * a one-CTA prep kernel turns cu_seqlens [R, E+B+1] into a list of m-tiles
-//     (128 receive rows sharing one weight row); the host never learns the
-//     segment sizes (no host synchronisation);
-//   * a persistent kernel, one CTA per SM, strides over (m-tile, n-tile) work
-//     units, n fastest so that neighbouring CTAs share the A tile and a weight
-//     row's column blocks stay in L2 while its m-tiles pass;
-//   * warp 0 issues TMA loads (A: 128 x 64 bf16, K-major, 128-byte swizzle;
-//     B: 64 x BN bf16 in 64-column chunks, N contiguous = MN-major, 128-byte
-//     swizzle) into a 4-stage shared-memory ring guarded by mbarriers;
-//   * warp 1 (one thread) issues tcgen05.mma.kind::f16 (M=128, N=BN, K=16,
-//     bf16 in, fp32 accumulate) into one of two TMEM accumulators, and
-//     tcgen05.commit frees each stage and publishes each finished tile;
-//   * warps 2..5 drain the other accumulator (tcgen05.ld 32x32b), round to
-//     bf16 (nearest even) and store only the rows inside the segment, so a
-//     tile never writes into the next segment.
+//   * a one-CTA prep kernel turns cu_seqlens [R, E+B+1] into a work list on the
+//     device (FWD/DX: m-tiles of 128 rows sharing a weight row; DW: one entry
+//     per non-empty segment), so the host never learns segment sizes;
+//   * a persistent kernel, one CTA per SM, strides over work units with the n
+//     tile fastest, so neighbouring CTAs share their A tile in L2;
+//   * warp 0 issues TMA loads (128-byte swizzle) into a 4-stage shared-memory
+//     ring guarded by mbarriers;
+//   * warp 1 (one thread) issues tcgen05.mma.kind::f16 (M=128, N=BN<=256, K=16,
+//     bf16 in, fp32 accumulate) into one of two TMEM accumulators; tcgen05.commit
+//     frees each stage and publishes each finished tile;
+//   * 4 (DW: 8) epilogue warps drain the other accumulator with tcgen05.ld:
+//     FWD/DX round to bf16 (nearest even) and store only the rows inside the
+//     segment; DW adds the fp32 tile into the gradient rows;
+//   * DW only: a segment's last K block usually extends past the segment, into
+//     the next segment's rows; a fix-up warp zeroes those rows of both operand
+//     tiles in shared memory before the MMA may read them.
 // Every mbarrier wait is bounded (2 s on the global timer); on expiry the CTA
 // records BEP_DERR_TIMEOUT, every role leaves its loop, and TMEM is freed.
 
@@ -35,10 +44,21 @@ namespace bep {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBChunkBytes = 64 * kBK * 2;      // 8 KB: 64 K-rows x 64 N columns
+constexpr int kBChunkBytes = 64 * kBK * 2;      // 8 KB: 64 rows x 64 columns of bf16
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2 };
+
+template <int MODE>
+struct ModeCfg {
+    static constexpr bool kAmn = MODE == kDw;          // A operand MN-major (recv^T)
+    static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
+    static constexpr bool kFix = MODE == kDw;          // tail-zeroing warp
+    static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
+    static constexpr int kWarps = 2 + kEpiWarps + (kFix ? 1 : 0);
+    static constexpr int kThreads = 32 * kWarps;
+};
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -123,11 +143,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
-// B MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Operand descriptor for the 16-deep K step kk of a 64-deep stage.
+//   K-major tile (rows x 64 K, 128-byte rows): 8-row groups 1024 B apart; a
+//   K step advances 32 B inside the swizzled row.
+//   MN-major tile (64 K-rows x 64-column chunks, 8 KB per chunk): chunks 8 KB
+//   apart along M/N, 8-row K groups 1024 B apart; a K step is 16 rows = 2048 B.
+template <bool kMN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+    return kMN ? sdesc_sw128(base + kk * 2048, kBChunkBytes, 1024)
+               : sdesc_sw128(base + kk * 32, 16, 1024);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B major
+// bits 15/16 (1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -170,9 +201,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// ---------------------------------------------------------------- tile list
+// ---------------------------------------------------------------- work list
+// seg_mode == 0: m-tiles of <= 128 rows per non-empty segment (FWD, DX);
+// seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
-                                                          Workspace ws) {
+                                                          Workspace ws, int seg_mode) {
     __shared__ int s_warp[33];
     const int n_items = d.R * d.NROW;
     const int per = (n_items + blockDim.x - 1) / blockDim.x;
@@ -187,6 +220,7 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         }
         *start = a;
         *len = b - a;
+        if (seg_mode) return b > a ? 1 : 0;
         return (b - a + kBM - 1) / kBM;
     };
     int sum = 0;
@@ -225,7 +259,7 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         for (int m = 0; m < n; ++m) {
             MTile t;
             t.row0 = (int32_t)(u * d.C + s + m * kBM);
-            t.rows = min(kBM, l - m * kBM);
+            t.rows = seg_mode ? l : min(kBM, l - m * kBM);
             t.wsel = wsel;
             t.pad = 0;
             ws.tiles[run + m] = t;
@@ -236,36 +270,87 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
     if (threadIdx.x == 0) *ws.ntiles = total <= d.max_tiles ? total : 0;
 }
 
+struct GemmParams {
+    const MTile* tiles;
+    const int32_t* ntiles;
+    uint16_t* out;       // FWD / DX: bf16 [R*C, N]
+    float* g_home;       // DW: [E, H, H'] fp32
+    float* red;          // DW: [R*B, H, H'] fp32
+    int N;               // output columns
+    int Kdim;            // FWD / DX: reduction length (H / H')
+    int H;               // rows of one expert's weight block
+    int BN;
+    int tmem_cols;
+    int mtd;             // DW: m-blocks per weight row (H / 128)
+    int32_t* status;
+};
+
+// Units of work, identical for every role of a CTA.
+struct Unit {
+    MTile t;
+    int nt;
+    int mblk;   // DW: m-block inside the [H, H'] gradient
+    int kb_n;   // K blocks of 64
+    int tail;   // DW: valid rows of the last K block (64 = full)
+};
+
+template <int MODE>
+__device__ __forceinline__ Unit unit_at(const GemmParams& p, int unit, int NT) {
+    Unit u;
+    if (MODE == kDw) {
+        const int per = p.mtd * NT;
+        const int seg = unit / per;
+        const int rem = unit - seg * per;
+        u.t = p.tiles[seg];
+        u.mblk = rem / NT;
+        u.nt = rem - u.mblk * NT;
+        u.kb_n = (u.t.rows + kBK - 1) / kBK;
+        u.tail = u.t.rows - (u.kb_n - 1) * kBK;
+    } else {
+        const int mt = unit / NT;
+        u.t = p.tiles[mt];
+        u.nt = unit - mt * NT;
+        u.mblk = 0;
+        u.kb_n = p.Kdim / kBK;
+        u.tail = kBK;
+    }
+    return u;
+}
+
 // ---------------------------------------------------------------- the GEMM
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
-    const __grid_constant__ CUtensorMap tmBs, const MTile* __restrict__ tiles,
-    const int32_t* __restrict__ ntiles_ptr, uint16_t* __restrict__ y, int H, int Hp, int BN,
-    int tmem_cols, int32_t* status) {
+template <int MODE>
+__global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+    const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+    using CF = ModeCfg<MODE>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned carve-up: A ring, B ring, barriers
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const int BN = p.BN;
     const int b_bytes = BN * kBK * 2;
     uint8_t* smA = smem;
     uint8_t* smB = smem + kStages * kABytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smB + kStages * b_bytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
-    uint64_t* tfull = bars + 2 * kStages;
-    uint64_t* tempty = bars + 2 * kStages + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    uint64_t* fix = bars + 2 * kStages;
+    uint64_t* tfull = bars + 3 * kStages;
+    uint64_t* tempty = bars + 3 * kStages + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int32_t* status = p.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&fix[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], CF::kEpiWarps);
         }
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -273,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(s_tmem)),
-                     "r"(tmem_cols)
+                     "r"(p.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -282,12 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
-    const int ntiles = *ntiles_ptr;
-    const int NT = Hp / BN;
-    const int total = ntiles * NT;
-    const int KB = H / kBK;
+    const int NT = p.N / BN;
+    const int total = MODE == kDw ? *p.ntiles * p.mtd * NT : *p.ntiles * NT;
     const uint32_t stage_bytes = (uint32_t)(kABytes + b_bytes);
-    const int acc_stride = tmem_cols / 2;   // two accumulators, power-of-two spaced columns
+    const int acc_stride = p.tmem_cols / 2;   // two accumulators, power-of-two spaced columns
 
     if (warp == 0) {
         if (lane == 0) {
@@ -296,21 +379,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             uint32_t s = 0, ph = 0;
             bool live = true;
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
-                const int mt = unit / NT, nt = unit - (unit / NT) * NT;
-                const MTile t = tiles[mt];
-                const CUtensorMap* tmB = t.wsel >= 0 ? &tmBh : &tmBs;
-                const int brow0 = (t.wsel >= 0 ? t.wsel : (-1 - t.wsel)) * H;
-                const int n0 = nt * BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                const Unit u = unit_at<MODE>(p, unit, NT);
+                const int n0 = u.nt * BN;
+                const CUtensorMap* tmB = (MODE == kDw || u.t.wsel >= 0) ? &tmB0 : &tmB1;
+                const int brow0 = (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel)) * p.H;
+                for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d(&tmA, &full[s], smA + s * kABytes, kb * kBK, t.row0);
-                    for (int c = 0; c < BN / 64; ++c)
-                        tma_load_2d(tmB, &full[s], smB + s * b_bytes + c * kBChunkBytes, n0 + c * 64,
-                                    brow0 + kb * kBK);
+                    uint8_t* a_dst = smA + s * kABytes;
+                    uint8_t* b_dst = smB + s * b_bytes;
+                    if (MODE == kFwd) {
+                        tma_load_2d(&tmA, &full[s], a_dst, kb * kBK, u.t.row0);
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_2d(tmB, &full[s], b_dst + c * kBChunkBytes, n0 + c * 64,
+                                        brow0 + kb * kBK);
+                    } else if (MODE == kDx) {
+                        tma_load_2d(&tmA, &full[s], a_dst, kb * kBK, u.t.row0);
+                        tma_load_2d(tmB, &full[s], b_dst, kb * kBK, brow0 + n0);
+                    } else {
+                        const int r0 = u.t.row0 + kb * kBK;
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d(&tmA, &full[s], a_dst + c * kBChunkBytes,
+                                        u.mblk * kBM + c * 64, r0);
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_2d(&tmB0, &full[s], b_dst + c * kBChunkBytes, n0 + c * 64, r0);
+                    }
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -321,18 +417,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_bf16(kBM, BN);
+            const uint32_t idesc = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
             uint32_t s = 0, ph = 0;
             bool live = true;
             int it = 0;
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
+                const Unit u = unit_at<MODE>(p, unit, NT);
                 const int acc = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&full[s], ph, s_abort, status)) {
+                        live = false;
+                        break;
+                    }
+                    // DW: the fix-up warp releases every stage (after zeroing a tail),
+                    // once per use, so fix[s] runs in the same phase as full[s].
+                    if (CF::kFix && !mbar_wait(&fix[s], ph, s_abort, status)) {
                         live = false;
                         break;
                     }
@@ -340,13 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
                     const uint32_t a0 = smem_u32(smA + s * kABytes);
                     const uint32_t b0 = smem_u32(smB + s * b_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // A: K-major, advance 16 elements (32 B) inside the 128-byte swizzle row.
-                        // B: MN-major, advance 16 K-rows = two 8-row groups of 1024 B.
-                        const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(b0 + kk * 2048, kBChunkBytes, 1024);
-                        mma_bf16(dt, ad, bd, idesc, (kb | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
+                                 idesc, (kb | kk) != 0);
                     mma_commit(&empty[s]);
                     if (++s == kStages) {
                         s = 0;
@@ -356,9 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
                 if (live) mma_commit(&tfull[acc]);
             }
         }
-    } else {
-        // ---------------------------------------------------- epilogue (warps 2..5)
-        const int q = warp & 3;   // TMEM lanes 32q..32q+31 are this warp's
+    } else if (warp < 2 + CF::kEpiWarps) {
+        // ---------------------------------------------------- epilogue
+        const int e = warp - 2;
+        const int q = warp & 3;                            // TMEM lanes 32q..32q+31 are this warp's
+        const int halves = CF::kEpiWarps / 4;              // warps sharing one lane quadrant
+        const int cspan = BN / halves;
+        const int c_lo = (e / 4) * cspan;
         int it = 0;
         for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -367,31 +470,96 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            const int mt = unit / NT, nt = unit - (unit / NT) * NT;
-            const MTile t = tiles[mt];
+            const Unit u = unit_at<MODE>(p, unit, NT);
             const int row = q * 32 + lane;
-            const bool valid = row < t.rows;
-            uint16_t* yrow = y + (int64_t)(t.row0 + row) * Hp + (int64_t)nt * BN;
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(
-                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_stride + c0), r);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + c0);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_stride);
+            if (MODE == kDw) {
+                float* out = (u.t.wsel >= 0 ? p.g_home + (int64_t)u.t.wsel * p.H * p.N
+                                            : p.red + (int64_t)(-1 - u.t.wsel) * p.H * p.N);
+                float4* orow = reinterpret_cast<float4*>(
+                    out + (int64_t)(u.mblk * kBM + row) * p.N + (int64_t)u.nt * BN);
+                for (int c0 = c_lo; c0 < c_lo + cspan; c0 += 32) {
+                    float4 old[8];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                        o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                        o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                        o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                        dst[v] = o;
+                    for (int v = 0; v < 8; ++v) old[v] = orow[c0 / 4 + v];
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float4 o = old[v];
+                        o.x = __fadd_rn(o.x, __uint_as_float(r[4 * v + 0]));
+                        o.y = __fadd_rn(o.y, __uint_as_float(r[4 * v + 1]));
+                        o.z = __fadd_rn(o.z, __uint_as_float(r[4 * v + 2]));
+                        o.w = __fadd_rn(o.w, __uint_as_float(r[4 * v + 3]));
+                        orow[c0 / 4 + v] = o;
+                    }
+                }
+            } else {
+                const bool valid = row < u.t.rows;
+                uint16_t* yrow = p.out + (int64_t)(u.t.row0 + row) * p.N + (int64_t)u.nt * BN;
+                for (int c0 = c_lo; c0 < c_lo + cspan; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            dst[v] = o;
+                        }
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    } else if (CF::kFix) {
+        // ---------------------------------------------------- tail fix-up (DW)
+        // The last K block of a segment holds rows of the next segment past
+        // `tail`; zero them in both operand tiles (whole 128-byte rows, so the
+        // swizzle does not matter) before the MMA reads the stage. The warp
+        // takes part in every stage (waits full[s], releases fix[s]) so it can
+        // never drift a whole phase away from the ring: a parity wait only
+        // tells apart two consecutive phases.
+        uint32_t s = 0, ph = 0;
+        bool live = true;
+        for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
+            const Unit u = unit_at<MODE>(p, unit, NT);
+            for (int kb = 0; kb < u.kb_n; ++kb) {
+                const bool got = mbar_wait(&full[s], ph, s_abort, status);
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, got)) {
+                    live = false;
+                    break;
+                }
+                if (kb == u.kb_n - 1 && u.tail < kBK) {
+                    const int nrow = kBK - u.tail;
+                    const int nchunk = 2 + BN / 64;            // A: 2 chunks, B: BN/64 chunks
+                    const int n16 = nrow * 8 * nchunk;         // 16-byte pieces to clear
+                    for (int i = lane; i < n16; i += 32) {
+                        const int piece = i & 7;
+                        const int rc = i >> 3;
+                        const int r = u.tail + rc % nrow;
+                        const int c = rc / nrow;
+                        uint8_t* base = c < 2 ? smA + s * kABytes + c * kBChunkBytes
+                                              : smB + s * b_bytes + (c - 2) * kBChunkBytes;
+                        *reinterpret_cast<uint4*>(base + r * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    // generic-proxy stores become visible to the tensor core's async proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&fix[s]);
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
         }
     }
 
@@ -403,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(tmem_cols)
+                     "r"(p.tmem_cols)
                      : "memory");
     }
 }
@@ -437,14 +605,28 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
     return r == CUDA_SUCCESS;
 }
 
-int pick_bn(int Hp) {
+int pick_bn(int n) {
     for (int bn = 256; bn >= 64; bn -= 64)
-        if (Hp % bn == 0) return bn;
+        if (n % bn == 0) return bn;
     return 64;
 }
 
 size_t smem_bytes(int BN) {
-    return 1024 + (size_t)kStages * (kABytes + BN * kBK * 2) + (2 * kStages + 4) * 8 + 16;
+    return 1024 + (size_t)kStages * (kABytes + BN * kBK * 2) + (3 * kStages + 4) * 8 + 16;
+}
+
+int tmem_cols_for(int BN) {
+    int c = 32;
+    while (c < 2 * BN) c <<= 1;
+    return c;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const GemmParams& prm, int num_sms, cudaStream_t st) {
+    grouped_gemm_kernel<MODE><<<num_sms, ModeCfg<MODE>::kThreads, smem_bytes(prm.BN), st>>>(a, b0, b1,
+                                                                                             prm);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -453,8 +635,12 @@ cudaError_t gemm_setup(int device) {
     (void)device;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes(256));
+    const int sm = (int)smem_bytes(256);
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(grouped_gemm_kernel<kDw>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
 }
 
 cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -464,7 +650,7 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     if (d.C == 0) return cudaSuccess;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws);
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
     const int BN = pick_bn(d.Hp);
     CUtensorMap tmA, tmBh, tmBs;
     if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBM, kBK)) return cudaErrorInvalidValue;
@@ -472,11 +658,75 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     const uint64_t slot_rows = (uint64_t)(d.R * d.B > 0 ? d.R * d.B : 1) * d.H;
     if (!encode_2d(&tmBs, w_slots ? w_slots : w_home, slot_rows, d.Hp, kBK, 64))
         return cudaErrorInvalidValue;
-    int tmem_cols = 32;
-    while (tmem_cols < 2 * BN) tmem_cols <<= 1;
-    grouped_gemm_kernel<<<num_sms, kThreads, smem_bytes(BN), st>>>(
-        tmA, tmBh, tmBs, ws.tiles, ws.ntiles, y, d.H, d.Hp, BN, tmem_cols, ws.status);
-    return cudaGetLastError();
+    GemmParams prm = {};
+    prm.tiles = ws.tiles;
+    prm.ntiles = ws.ntiles;
+    prm.out = y;
+    prm.N = d.Hp;
+    prm.Kdim = d.H;
+    prm.H = d.H;
+    prm.BN = BN;
+    prm.tmem_cols = tmem_cols_for(BN);
+    prm.mtd = 1;
+    prm.status = ws.status;
+    return launch_mode<kFwd>(tmA, tmBh, tmBs, prm, num_sms, st);
+}
+
+cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* dy, const uint16_t* w_home,
+                                   const uint16_t* w_slots, uint16_t* drecv, int num_sms,
+                                   cudaStream_t st) {
+    if (d.C == 0) return cudaSuccess;
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
+    const int BN = pick_bn(d.H);
+    CUtensorMap tmA, tmBh, tmBs;
+    // A: dY [R*C, H'] rows, 64-wide K boxes; B: W rows h (N) x 64 columns h' (K)
+    if (!encode_2d(&tmA, dy, (uint64_t)d.R * d.C, d.Hp, kBM, kBK)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tmBh, w_home, (uint64_t)d.E * d.H, d.Hp, BN, kBK)) return cudaErrorInvalidValue;
+    const uint64_t slot_rows = (uint64_t)(d.R * d.B > 0 ? d.R * d.B : 1) * d.H;
+    if (!encode_2d(&tmBs, w_slots ? w_slots : w_home, slot_rows, d.Hp, BN, kBK))
+        return cudaErrorInvalidValue;
+    GemmParams prm = {};
+    prm.tiles = ws.tiles;
+    prm.ntiles = ws.ntiles;
+    prm.out = drecv;
+    prm.N = d.H;
+    prm.Kdim = d.Hp;
+    prm.H = d.H;
+    prm.BN = BN;
+    prm.tmem_cols = tmem_cols_for(BN);
+    prm.mtd = 1;
+    prm.status = ws.status;
+    return launch_mode<kDx>(tmA, tmBh, tmBs, prm, num_sms, st);
+}
+
+cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* recv, const uint16_t* dy, float* g_home,
+                                   float* red, int num_sms, cudaStream_t st) {
+    if (d.C == 0) return cudaSuccess;
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 1);
+    const int BN = pick_bn(d.Hp);
+    CUtensorMap tmA, tmB;
+    // A: recv^T in 64 (h) x 64 (row) boxes; B: dY in 64 (h') x 64 (row) boxes
+    if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBK, 64)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tmB, dy, (uint64_t)d.R * d.C, d.Hp, kBK, 64)) return cudaErrorInvalidValue;
+    GemmParams prm = {};
+    prm.tiles = ws.tiles;
+    prm.ntiles = ws.ntiles;
+    prm.g_home = g_home;
+    prm.red = red;
+    prm.N = d.Hp;
+    prm.Kdim = 0;
+    prm.H = d.H;
+    prm.BN = BN;
+    prm.tmem_cols = tmem_cols_for(BN);
+    prm.mtd = d.H / kBM;
+    prm.status = ws.status;
+    return launch_mode<kDw>(tmA, tmB, tmB, prm, num_sms, st);
 }
 
 }  // namespace bep

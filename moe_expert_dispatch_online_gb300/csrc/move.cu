@@ -106,8 +106,15 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restr
 }
 
 // ----------------------------------------------------------------------------- combine
-// out[tok, c] = bf16_rne(acc), acc = 0; for k in 0..K-1: acc = fma(g[tok,k], y[dest[tok,k], c], acc)
-template <int U>
+// kWeighted:  out[tok, c] = bf16_rne(acc), acc = 0; for k in 0..K-1:
+//             acc = fma(g[tok,k], y[dest[tok,k], c], acc)
+// !kWeighted (backward of the dispatch): acc = acc + y[dest[tok,k], c] instead.
+template <bool kWeighted>
+__device__ __forceinline__ float combine_step(float g, float v, float acc) {
+    return kWeighted ? __fmaf_rn(g, v, acc) : __fadd_rn(acc, v);
+}
+
+template <int U, bool kWeighted>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ y,
                                                            const int32_t* __restrict__ dest,
                                                            const float* __restrict__ gates,
@@ -120,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
          tok += nwarps) {
         unsigned okmask;
         const int dl = load_dest(dest, tok, K, nrows, &okmask, status);
-        const float gl = lane < K ? gates[tok * K + lane] : 0.0f;
+        const float gl = (kWeighted && lane < K) ? gates[tok * K + lane] : 1.0f;
         for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
             float acc[U][8];
 #pragma unroll
@@ -151,10 +158,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                     float f[8];
                     bf16x8_to_f32(q0[u], f);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = __fmaf_rn(g0, f[i], acc[u][i]);
+                    for (int i = 0; i < 8; ++i) acc[u][i] = combine_step<kWeighted>(g0, f[i], acc[u][i]);
                     bf16x8_to_f32(q1[u], f);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = __fmaf_rn(g1, f[i], acc[u][i]);
+                    for (int i = 0; i < 8; ++i) acc[u][i] = combine_step<kWeighted>(g1, f[i], acc[u][i]);
                 }
             }
             if (k < K) {
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                     float f[8];
                     bf16x8_to_f32(q, f);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = __fmaf_rn(g0, f[i], acc[u][i]);
+                    for (int i = 0; i < 8; ++i) acc[u][i] = combine_step<kWeighted>(g0, f[i], acc[u][i]);
                 }
             }
 #pragma unroll
@@ -401,9 +408,19 @@ cudaError_t launch_combine(const Dims& d, const Workspace& ws, const uint16_t* y
                            int num_sms, cudaStream_t st) {
     const int64_t ntok = (int64_t)d.R * d.S;
     if (ntok == 0) return cudaSuccess;
-    combine_kernel<4><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+    combine_kernel<4, true><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(y), dest, gates, reinterpret_cast<uint4*>(out), ntok, d.K,
         D / 8, (int64_t)d.R * d.C, ws.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_bwd(const Dims& d, const Workspace& ws, const uint16_t* drecv,
+                                const int32_t* dest, uint16_t* dx, int num_sms, cudaStream_t st) {
+    const int64_t ntok = (int64_t)d.R * d.S;
+    if (ntok == 0) return cudaSuccess;
+    combine_kernel<4, false><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(drecv), dest, nullptr, reinterpret_cast<uint4*>(dx), ntok,
+        d.K, d.H / 8, (int64_t)d.R * d.C, ws.status);
     return cudaGetLastError();
 }
 

@@ -82,6 +82,8 @@ def _load():
                 "oracle_dispatch": (None, [u16p, i32p, ci, ci, ci, ci, u16p]),
                 "oracle_combine": (None, [u16p, i32p, f32p, ci, ci, ci, ci, u16p]),
                 "oracle_combine_bwd": (None, [u16p, i32p, f32p, ci, ci, ci, ci, u16p]),
+                "oracle_dispatch_bwd": (None, [u16p, i32p, ci, ci, ci, ci, u16p]),
+                "oracle_combine_dgates": (None, [u16p, u16p, i32p, ci, ci, ci, ci, f64p]),
                 "oracle_prefetch": (None, [u16p, i32p, ci, ci, c64, u16p]),
                 "oracle_reduce_grad": (None, [f32p, f32p, i32p, ci, ci, ci, c64]),
             }
@@ -312,3 +314,73 @@ def weight_row_of(rho: int, u: int, E: int, slot_expert: np.ndarray) -> int:
     """The home expert whose weights serve segment row rho on rank u: rho itself for
     rho < E, else the expert prefetch_weight copied into slot rho - E."""
     return int(rho) if rho < E else int(slot_expert[u, rho - E])
+
+
+def dispatch_bwd(drecv: np.ndarray, dest: np.ndarray) -> np.ndarray:
+    """drecv uint16 [R*S*K, H], dest [R,S,K] -> dx uint16 [R,S,H] (sum of the K rows, fp32, in k order)."""
+    drecv = np.ascontiguousarray(drecv, dtype=np.uint16)
+    dest = np.ascontiguousarray(dest, dtype=np.int32)
+    R, S, K = dest.shape
+    H = drecv.shape[1]
+    dx = np.zeros((R, S, H), np.uint16)
+    _load().oracle_dispatch_bwd(_ptr(drecv, ctypes.c_uint16), _ptr(dest, ctypes.c_int32), R, S, K,
+                                H, _ptr(dx, ctypes.c_uint16))
+    return dx
+
+
+def combine_dgates(dout: np.ndarray, y: np.ndarray, dest: np.ndarray) -> np.ndarray:
+    """dg [R,S,K] float64: <dOut[r,t], Y[dest[r,t,k]]>."""
+    dout = np.ascontiguousarray(dout, dtype=np.uint16)
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    dest = np.ascontiguousarray(dest, dtype=np.int32)
+    R, S, K = dest.shape
+    D = y.shape[1]
+    dg = np.zeros((R, S, K), np.float64)
+    _load().oracle_combine_dgates(_ptr(dout, ctypes.c_uint16), _ptr(y, ctypes.c_uint16),
+                                  _ptr(dest, ctypes.c_int32), R, S, K, D,
+                                  _ptr(dg, ctypes.c_double))
+    return dg
+
+
+def grouped_gemm_dx(dy: np.ndarray, w_home: np.ndarray, w_slots: np.ndarray, cu: np.ndarray,
+                    E: int) -> np.ndarray:
+    """Input gradient of the expert GEMM, binary64: for every non-empty segment,
+    dRecv[u, seg] = dY[u, seg] @ W(u, rho)^T (W(u, rho) as in grouped_gemm)."""
+    R = cu.shape[0]
+    nrow_total = dy.shape[0]
+    C = nrow_total // R
+    H = w_home.shape[1]
+    out = np.zeros((nrow_total, H), np.float64)
+    for u in range(R):
+        for rho in range(cu.shape[1] - 1):
+            a, b = int(cu[u, rho]), int(cu[u, rho + 1])
+            if b == a:
+                continue
+            w = w_home[rho] if rho < E else w_slots[u, rho - E]
+            G = bf16_to_f32(dy[u * C + a:u * C + b]).astype(np.float64)
+            W = bf16_to_f32(w).astype(np.float64)
+            out[u * C + a:u * C + b] = G @ W.T
+    return out
+
+
+def grouped_gemm_dw(recv: np.ndarray, dy: np.ndarray, cu: np.ndarray, E: int, B: int,
+                    H: int, Hp: int):
+    """Weight gradient of the expert GEMM, binary64, per non-empty segment:
+    dW(u, rho) = recv[u, seg]^T @ dY[u, seg]. Returns (d_home [E,H,H'], d_slots [R,B,H,H']),
+    summing the segments that share a weight row (a home row's segments on every rank)."""
+    R = cu.shape[0]
+    C = recv.shape[0] // R
+    d_home = np.zeros((E, H, Hp), np.float64)
+    d_slots = np.zeros((R, B, H, Hp), np.float64)
+    for u in range(R):
+        for rho in range(cu.shape[1] - 1):
+            a, b = int(cu[u, rho]), int(cu[u, rho + 1])
+            if b == a:
+                continue
+            A = bf16_to_f32(recv[u * C + a:u * C + b]).astype(np.float64)
+            G = bf16_to_f32(dy[u * C + a:u * C + b]).astype(np.float64)
+            if rho < E:
+                d_home[rho] += A.T @ G
+            else:
+                d_slots[u, rho - E] += A.T @ G
+    return d_home, d_slots

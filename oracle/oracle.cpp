@@ -446,6 +446,39 @@ void oracle_combine_bwd(const uint16_t* dout, const int32_t* dest, const float* 
         }
 }
 
+// Backward of the dispatch (a copy of each token to K rows): the token's
+// gradient is the sum of its K receive-row gradients,
+// dx[r,t,c] = bf16_rne(acc), acc = 0; for k = 0..K-1: acc = acc + dRecv[dest[r,t,k], c]
+// (fp32 adds in ascending k).
+void oracle_dispatch_bwd(const uint16_t* drecv, const int32_t* dest, int R, int S, int K, int H,
+                         uint16_t* dx) {
+    int64_t ntok = (int64_t)R * S;
+    for (int64_t tok = 0; tok < ntok; ++tok)
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int64_t d = dest[tok * K + k];
+                acc = acc + bf16_to_f32(drecv[d * H + c]);
+            }
+            dx[tok * H + c] = f32_to_bf16_rne(acc);
+        }
+}
+
+// Gradient of the combine with respect to the gates:
+// dg[r,t,k] = sum_c dOut[r,t,c] * Y[dest[r,t,k], c], accumulated in binary64.
+void oracle_combine_dgates(const uint16_t* dout, const uint16_t* y, const int32_t* dest, int R,
+                           int S, int K, int D, double* dg) {
+    int64_t ntok = (int64_t)R * S;
+    for (int64_t tok = 0; tok < ntok; ++tok)
+        for (int k = 0; k < K; ++k) {
+            int64_t d = dest[tok * K + k];
+            double acc = 0.0;
+            for (int c = 0; c < D; ++c)
+                acc += (double)bf16_to_f32(dout[tok * D + c]) * (double)bf16_to_f32(y[d * D + c]);
+            dg[tok * K + k] = acc;
+        }
+}
+
 // prefetch_weight: slots[u][j] <- W_home[slot_expert[u][j]] for every used
 // slot ([P4] "The memory contract": rows [E, E+B) are local prefetch slots).
 void oracle_prefetch(const uint16_t* w_home, const int32_t* slot_expert, int R, int B,

@@ -1,0 +1,223 @@
+"""GPU parity of the backward path (through the C ABI) against the oracle:
+dispatch backward bit-exact (fp32 adds in k order); the input-gradient GEMM
+(dRecv = dY W^T) within 2e-2 relative per segment; the weight-gradient GEMM
+(dW = recv^T dY, accumulated into g_home rows and the red reduce buffer)
+within 2e-2 relative per weight row, with rows outside the plan unchanged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+RTOL = 2e-2
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(DEV).view(
+        torch.bfloat16)
+
+
+def host_u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def setup(bep, name, target, seed=0):
+    wl = synth.WORKLOADS[name]
+    topk = synth.routing(wl, target, seed)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    cfg = bep.Config(wl.R, wl.E, wl.B, wl.K, wl.S, wl.H, wl.Hp, wl.mode)
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, DEV)
+    bep.bep_plan(ctx, torch.from_numpy(topk).to(DEV), buf.cu_seqlens, buf.slot_expert, buf.dest,
+                 buf.maxvio)
+    np.testing.assert_array_equal(buf.dest.cpu().numpy(), ref.dest)
+    np.testing.assert_array_equal(buf.cu_seqlens.cpu().numpy(), ref.cu)
+    return wl, ref, ctx, buf
+
+
+@pytest.mark.parametrize("name,target", [("tiny_r2_e8", None), ("train_r8_e64", 10.0),
+                                         ("grad_r8_e64", 10.0)])
+def test_dispatch_bwd_bit_exact(lib, name, target):
+    bep = lib
+    wl, ref, ctx, buf = setup(bep, name, target)
+    drecv = synth.tokens_host((wl.R * wl.C, wl.H), 51)
+    dx_ref = oracle.dispatch_bwd(drecv, ref.dest)
+    dx = torch.empty((wl.R, wl.S, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_dispatch_bwd(ctx, dev_u16(drecv), buf.dest, dx)
+    assert bep.bep_status(ctx) == 0
+    np.testing.assert_array_equal(host_u16(dx), dx_ref)
+
+
+def test_dispatch_bwd_bench_size_sampled(lib):
+    bep = lib
+    wl, ref, ctx, buf = setup(bep, "bench_r8_e384", 20.0)
+    drecv = synth.tokens_device((wl.R * wl.C, wl.H), 52)
+    dx = torch.empty((wl.R, wl.S, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_dispatch_bwd(ctx, drecv, buf.dest, dx)
+    assert bep.bep_status(ctx) == 0
+    toks = np.random.default_rng(3).choice(wl.R * wl.S, size=1024, replace=False)
+    d = ref.dest.reshape(-1, wl.K)[toks]
+    rows = host_u16(drecv[torch.from_numpy(d.ravel().astype(np.int64)).to(DEV)])
+    local = np.arange(len(toks) * wl.K, dtype=np.int32).reshape(1, len(toks), wl.K)
+    exp = oracle.dispatch_bwd(rows, local)[0]
+    got = host_u16(dx.view(-1, wl.H)[torch.from_numpy(toks).to(DEV)])
+    np.testing.assert_array_equal(got, exp)
+
+
+def _segments(ref, R, E, B):
+    for u in range(R):
+        for rho in range(E + B):
+            a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+            if b > a:
+                yield u, rho, a, b
+
+
+@pytest.mark.parametrize("name,target", [("tiny_r2_e8", None), ("train_r8_e64", 10.0),
+                                         ("grad_r8_e64", 10.0)])
+def test_grouped_gemm_dx(lib, name, target):
+    bep = lib
+    wl, ref, ctx, buf = setup(bep, name, target)
+    w_home = synth.weights_host((wl.E, wl.H, wl.Hp), 61)
+    slots_ref = oracle.prefetch(w_home, ref.slot_expert, np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.uint16))
+    dy = synth.tokens_host((wl.R * wl.C, wl.Hp), 62)
+    dr_ref = oracle.grouped_gemm_dx(dy, w_home, slots_ref, ref.cu, wl.E)
+    w_home_d = dev_u16(w_home)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home_d, w_slots)
+    drecv = torch.empty((wl.R * wl.C, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, dev_u16(dy), w_home_d, w_slots, drecv)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    got = oracle.bf16_to_f32(host_u16(drecv)).astype(np.float64)
+    C = wl.C
+    worst = 0.0
+    for u, rho, a, b in _segments(ref, wl.R, wl.E, wl.B):
+        yr, yg = dr_ref[u * C + a:u * C + b], got[u * C + a:u * C + b]
+        err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
+        worst = max(worst, err)
+        assert err <= RTOL, (u, rho, err)
+    print(f"dx {name}: worst segment rel err {worst:.3e}")
+
+
+@pytest.mark.parametrize("name,target,g0", [("tiny_r2_e8", None, "zero"),
+                                            ("train_r8_e64", 10.0, "zero"),
+                                            ("train_r8_e64", 1.0, "random"),
+                                            ("grad_r8_e64", 10.0, "random")])
+def test_grouped_gemm_dw(lib, name, target, g0):
+    bep = lib
+    wl, ref, ctx, buf = setup(bep, name, target)
+    x = synth.tokens_host((wl.R, wl.S, wl.H), 71)
+    recv_ref = oracle.dispatch(x, ref.dest)
+    dy = synth.tokens_host((wl.R * wl.C, wl.Hp), 72)
+    d_home, d_slots = oracle.grouped_gemm_dw(recv_ref, dy, ref.cu, wl.E, wl.B, wl.H, wl.Hp)
+    if g0 == "zero":
+        G0 = np.zeros((wl.E, wl.H, wl.Hp), np.float32)
+        red0 = np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.float32)
+    else:
+        G0 = synth.normal_host((wl.E, wl.H, wl.Hp), 73, 0.5)
+        red0 = synth.normal_host((wl.R, wl.B, wl.H, wl.Hp), 74, 0.5)
+    bep.bep_dispatch(ctx, dev_u16(x), buf.dest, buf.recv)
+    g = torch.from_numpy(G0).to(DEV)
+    red = torch.from_numpy(red0).to(DEV)
+    bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, dev_u16(dy), g, red)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    gh, rh = g.cpu().numpy().astype(np.float64), red.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for e in range(wl.E):
+        want = G0[e] + d_home[e]
+        if not d_home[e].any():
+            np.testing.assert_array_equal(gh[e], G0[e])     # home segment empty: untouched
+            continue
+        err = np.linalg.norm(gh[e] - want) / max(np.linalg.norm(d_home[e]), 1e-30)
+        worst = max(worst, err)
+        assert err <= RTOL, (e, err)
+    for u in range(wl.R):
+        for j in range(wl.B):
+            want = red0[u, j] + d_slots[u, j]
+            if not d_slots[u, j].any():
+                np.testing.assert_array_equal(rh[u, j], red0[u, j])
+                continue
+            err = np.linalg.norm(rh[u, j] - want) / max(np.linalg.norm(d_slots[u, j]), 1e-30)
+            worst = max(worst, err)
+            assert err <= RTOL, (u, j, err)
+    print(f"dw {name} {g0}: worst row rel err {worst:.3e}")
+
+
+def test_grouped_gemm_dw_rejects_inference_mode(lib):
+    bep = lib
+    wl = synth.WORKLOADS["infer_r8_e384_b4"]
+    cfg = bep.Config(wl.R, wl.E, wl.B, wl.K, 64, wl.H, wl.Hp, wl.mode)
+    ctx = bep.Context(cfg)
+    # the mode is checked before any pointer is looked at or anything is queued
+    rc = bep.load().bep_grouped_gemm_dw(ctx.handle, None, None, None, None, None, None)
+    assert rc == bep.BEP_ERR_MODE
+
+
+def test_backward_chain_matches_oracle(lib):
+    """combine_bwd -> dx GEMM -> dispatch_bwd gives the token gradient of the
+    forward chain; compared with the oracle's chain (bf16 roundings between stages
+    as in the library)."""
+    bep = lib
+    wl, ref, ctx, buf = setup(bep, "train_r8_e64", 10.0)
+    w_home = synth.weights_host((wl.E, wl.H, wl.Hp), 81)
+    slots_ref = oracle.prefetch(w_home, ref.slot_expert, np.zeros((wl.R, wl.B, wl.H, wl.Hp), np.uint16))
+    gates = synth.gates_host(wl.R, wl.S, wl.K, 82)
+    dout = synth.tokens_host((wl.R, wl.S, wl.Hp), 83)
+    dy_ref = oracle.combine_bwd(dout, ref.dest, gates)
+    dr_ref = oracle.f32_to_bf16(oracle.grouped_gemm_dx(dy_ref, w_home, slots_ref, ref.cu, wl.E))
+    dx_ref = oracle.bf16_to_f32(oracle.dispatch_bwd(dr_ref, ref.dest)).astype(np.float64)
+    w_home_d = dev_u16(w_home)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home_d, w_slots)
+    dy = torch.empty((wl.R * wl.C, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_combine_bwd(ctx, dev_u16(dout), buf.dest, torch.from_numpy(gates).to(DEV), dy)
+    np.testing.assert_array_equal(host_u16(dy), dy_ref)
+    drecv = torch.empty((wl.R * wl.C, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, dy, w_home_d, w_slots, drecv)
+    dx = torch.empty((wl.R, wl.S, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_dispatch_bwd(ctx, drecv, buf.dest, dx)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    got = oracle.bf16_to_f32(host_u16(dx)).astype(np.float64)
+    assert np.linalg.norm(got - dx_ref) / np.linalg.norm(dx_ref) <= RTOL
+
+
+def test_grouped_gemm_dw_bench_size_sampled(lib):
+    """Full-size weight gradient; the oracle recomputes sampled rows h of dW for a
+    few home and slot segments from the inputs (x via the oracle's dest, and dY)."""
+    bep = lib
+    torch.cuda.empty_cache()
+    wl, ref, ctx, buf = setup(bep, "bench_r8_e384", 10.0)
+    x = synth.tokens_device((wl.R, wl.S, wl.H), 91)
+    dy = synth.tokens_device((wl.R * wl.C, wl.Hp), 92)
+    g = torch.zeros((wl.E, wl.H, wl.Hp), dtype=torch.float32, device=DEV)
+    red = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.float32, device=DEV)
+    bep.bep_dispatch(ctx, x, buf.dest, buf.recv)
+    bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, dy, g, red)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    C, E = wl.C, wl.E
+    inv = np.empty(wl.R * C, np.int64)
+    inv[ref.dest.ravel()] = np.arange(wl.R * wl.S * wl.K) // wl.K
+    segs = list(_segments(ref, wl.R, E, wl.B))
+    home = [s for s in segs if s[1] < E][:3]
+    slot = [s for s in segs if s[1] >= E][:3]
+    assert slot, "the maxvio-10 routing must use prefetch slots"
+    rng = np.random.default_rng(5)
+    for u, rho, a, b in home + slot:
+        gi = np.arange(u * C + a, u * C + b, dtype=np.int64)
+        xr = host_u16(x.view(-1, wl.H)[torch.from_numpy(inv[gi]).to(DEV)])
+        dyr = host_u16(dy[torch.from_numpy(gi).to(DEV)])
+        hs = np.concatenate([[0, wl.H - 1], rng.integers(0, wl.H, size=6)])
+        want = oracle.gemm_rows(np.ascontiguousarray(xr[:, hs].T), dyr)      # [len(hs), H']
+        out = g[rho] if rho < E else red[u, rho - E]
+        got = out[torch.from_numpy(hs).to(DEV)].cpu().numpy().astype(np.float64)
+        err = np.linalg.norm(got - want) / np.linalg.norm(want)
+        assert err <= RTOL, (u, rho, err)
+    del g, red, x, dy
+    torch.cuda.empty_cache()

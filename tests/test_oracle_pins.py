@@ -533,3 +533,125 @@ def test_grouped_gemm_brute_force_tiny():
                 acc += float(oracle.bf16_to_f32(recv[i:i + 1, h])[0]) * \
                        float(oracle.bf16_to_f32(w[h:h + 1, j])[0])
             assert abs(y[i, j] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+# ---------------------------------------------------------------- backward pieces
+def test_dispatch_bwd_k1_is_the_inverse_permutation():
+    topk, p, x, g, y = _small_problem(K=1, H=40)
+    R, S, H = x.shape
+    recv = oracle.dispatch(x, p.dest)
+    np.testing.assert_array_equal(oracle.dispatch_bwd(recv, p.dest), x)
+
+
+def test_dispatch_bwd_of_dispatch_is_K_times_x():
+    """Each token is copied to K rows; summing them back gives K*x, exact for K a
+    power of two (a scaling by 2^j), computed here by torch."""
+    topk, p, x, g, y = _small_problem(K=4, H=40)
+    recv = oracle.dispatch(x, p.dest)
+    dx = oracle.dispatch_bwd(recv, p.dest)
+    ref = torch.from_numpy(oracle.bf16_to_f32(x) * 4.0)
+    np.testing.assert_array_equal(dx, _torch_bf16_bits(ref.numpy()))
+
+
+def test_dispatch_bwd_exact_on_dyadic_values():
+    topk, p, x, g, y = _small_problem(K=4, H=16)
+    rng = np.random.default_rng(3)
+    v = rng.integers(-64, 65, size=(topk.size, 16)).astype(np.float32) / 8.0
+    drecv = _torch_bf16_bits(v)
+    dx = oracle.dispatch_bwd(drecv, p.dest)
+    exact = v[p.dest].astype(np.float64).sum(axis=2)
+    np.testing.assert_array_equal(dx, _torch_bf16_bits(exact.astype(np.float32)))
+
+
+def test_combine_dgates_brute_force():
+    topk, p, x, g, y = _small_problem(K=3, D=8, S=5)
+    R, S, K = topk.shape
+    dout = synth.tokens_host((R, S, 8), 4)
+    dg = oracle.combine_dgates(dout, y, p.dest)
+    yf, df = oracle.bf16_to_f32(y), oracle.bf16_to_f32(dout)
+    for r in range(R):
+        for t in range(S):
+            for k in range(K):
+                ref = sum(float(df[r, t, c]) * float(yf[p.dest[r, t, k], c]) for c in range(8))
+                assert abs(dg[r, t, k] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def _shift_weights(E, R, B, H, Hp):
+    def shift_w(s):
+        w = np.zeros((H, Hp), np.float32)
+        w[np.arange(H), (np.arange(H) + s) % Hp] = 1.0
+        return _torch_bf16_bits(w)
+    w_home = np.stack([shift_w(e) for e in range(E)])
+    w_slots = np.stack([np.stack([shift_w(E + u * B + j) for j in range(B)]) for u in range(R)])
+    return w_home, w_slots
+
+
+def test_grouped_gemm_dx_shift_matrices():
+    """dRecv = dY @ W^T with W_rho[h, j] = [j == (h + s_rho) mod H']: each output
+    element picks dY[i, (h + s_rho) mod H'], a distinct shift per weight row."""
+    R, S, K, E, H, Hp = 2, 23, 2, 8, 16, 8
+    B = E // R
+    topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 1.3), 5)
+    p = oracle.plan(topk, E, B, 0)
+    w_home, w_slots = _shift_weights(E, R, B, H, Hp)
+    dy = synth.tokens_host((R * S * K, Hp), 6)
+    dr = oracle.grouped_gemm_dx(dy, w_home, w_slots, p.cu, E)
+    C = S * K
+    df = oracle.bf16_to_f32(dy).astype(np.float64)
+    for i in range(R * C):
+        u, pos = divmod(i, C)
+        rho = int(np.searchsorted(p.cu[u], pos, side="right") - 1)
+        s = rho if rho < E else E + u * B + (rho - E)
+        np.testing.assert_array_equal(dr[i], df[i, (np.arange(H) + s) % Hp])
+
+
+def test_grouped_gemm_dw_brute_force_tiny():
+    R, S, K, E, H, Hp = 2, 6, 2, 4, 5, 3
+    B = E // R
+    topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 2.0), 2)
+    p = oracle.plan(topk, E, B, 0)
+    recv = synth.tokens_host((R * S * K, H), 7)
+    dy = synth.tokens_host((R * S * K, Hp), 8)
+    d_home, d_slots = oracle.grouped_gemm_dw(recv, dy, p.cu, E, B, H, Hp)
+    C = S * K
+    rf, df = oracle.bf16_to_f32(recv), oracle.bf16_to_f32(dy)
+    ref_home = np.zeros((E, H, Hp))
+    ref_slots = np.zeros((R, B, H, Hp))
+    for i in range(R * C):
+        u, pos = divmod(i, C)
+        rho = max(r for r in range(E + B) if p.cu[u][r] <= pos < p.cu[u][r + 1])
+        for h in range(H):
+            for j in range(Hp):
+                v = float(rf[i, h]) * float(df[i, j])
+                if rho < E:
+                    ref_home[rho, h, j] += v
+                else:
+                    ref_slots[u, rho - E, h, j] += v
+    np.testing.assert_allclose(d_home, ref_home, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(d_slots, ref_slots, rtol=1e-12, atol=1e-14)
+
+
+def test_grouped_gemm_dw_one_hot_rows_are_outer_products():
+    """recv rows that are one-hot at column h(i) make dW(rho)[h, :] the sum of the
+    dY rows of the segment whose one-hot column is h -- exact."""
+    R, S, K, E, H, Hp = 2, 17, 2, 8, 6, 4
+    B = E // R
+    topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 1.1), 9)
+    p = oracle.plan(topk, E, B, 0)
+    n = R * S * K
+    hot = np.arange(n) % H
+    recv = np.zeros((n, H), np.float32)
+    recv[np.arange(n), hot] = 1.0
+    dyv = np.random.default_rng(4).integers(-8, 9, size=(n, Hp)).astype(np.float32)
+    d_home, d_slots = oracle.grouped_gemm_dw(_torch_bf16_bits(recv), _torch_bf16_bits(dyv), p.cu,
+                                             E, B, H, Hp)
+    C = S * K
+    ref_home = np.zeros_like(d_home)
+    ref_slots = np.zeros_like(d_slots)
+    for i in range(n):
+        u, pos = divmod(i, C)
+        rho = int(np.searchsorted(p.cu[u], pos, side="right") - 1)
+        tgt = ref_home[rho] if rho < E else ref_slots[u, rho - E]
+        tgt[hot[i]] += dyv[i]
+    np.testing.assert_array_equal(d_home, ref_home)
+    np.testing.assert_array_equal(d_slots, ref_slots)
