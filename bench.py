@@ -195,6 +195,82 @@ def run_gpu(args, rank, world, local_rank):
     if st:
         raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
 
+    # ---- backward GEMMs and dispatch backward (rows beyond the step: measured apart)
+    bwd = None
+    if not args.no_backward:
+        drecv = torch.empty((R * S * K, H), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+        nb = min(args.steps, 2 * len(topks))
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+        nseg = []
+        for i in range(nb + 1):
+            step(i)            # plan, dispatch, GEMM, combine, combine_bwd for routing i
+            ev = bev[i - 1] if i > 0 else None
+            if ev is not None:
+                ev[0].record(stream)
+            bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, buf.dy, w_home, w_slots, drecv, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            bep.bep_dispatch_bwd(ctx, drecv, buf.dest, dx, stream)
+            if ev is not None:
+                ev[2].record(stream)
+            bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red, stream)
+            if ev is not None:
+                ev[3].record(stream)
+                nseg.append(int((buf.cu_seqlens[:, 1:] > buf.cu_seqlens[:, :-1]).sum().item()))
+        torch.cuda.synchronize()
+        st = bep.bep_status(ctx, stream)
+        if st:
+            raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+        dx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bev)
+        db_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in bev)
+        dw_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
+        flops = 2.0 * R * S * K * H * Hp
+        dw_bytes = statistics.mean(nseg) * H * Hp * 4 * 2 + R * S * K * (H + Hp) * 2
+        db_bytes = R * S * K * H * 2 + R * S * H * 2 + R * S * K * 4
+        bwd = {
+            "grouped_gemm_dx": {"ms": dx_ms, "tflops": flops / (dx_ms * 1e-3) / 1e12,
+                                "frac_bf16_sustained": flops / (dx_ms * 1e-3) / 1e12 / peaks()["bf16_sus"]},
+            "dispatch_bwd": {"ms": db_ms, "gbs": db_bytes / (db_ms * 1e-3) / 1e9,
+                             "frac_hbm": db_bytes / (db_ms * 1e-3) / 1e9 / peaks()["hbm"]},
+            "grouped_gemm_dw": {"ms": dw_ms, "tflops": flops / (dw_ms * 1e-3) / 1e12,
+                                "frac_bf16_sustained": flops / (dw_ms * 1e-3) / 1e12 / peaks()["bf16_sus"],
+                                "fp32_rmw_gbs": dw_bytes / (dw_ms * 1e-3) / 1e9,
+                                "segments": statistics.mean(nseg)},
+            "launches": nb,
+        }
+        del drecv, dx
+        torch.cuda.empty_cache()
+
+    # ---- dispatch + combine under a 32-SM budget (the pages' comm-SM setting)
+    comm32 = None
+    if not args.no_backward:
+        bep.bep_set_comm_sms(ctx, 32)
+        nb = min(args.steps, 2 * len(topks))
+        cev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb)]
+        for i in range(nb + 1):
+            bep.bep_plan(ctx, topks[i % len(topks)], buf.cu_seqlens, buf.slot_expert, buf.dest,
+                         buf.maxvio, stream)
+            ev = cev[i - 1] if i > 0 else None
+            if ev is not None:
+                ev[0].record(stream)
+            bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+            if ev is not None:
+                ev[2].record(stream)
+        torch.cuda.synchronize()
+        bep.bep_set_comm_sms(ctx, 0)
+        d32 = statistics.mean(e[0].elapsed_time(e[1]) for e in cev)
+        c32 = statistics.mean(e[1].elapsed_time(e[2]) for e in cev)
+        rh, rhp = H * 2, Hp * 2
+        db = R * S * rh + R * S * K * rh + R * S * K * 4
+        cb = R * S * K * rhp + R * S * rhp + R * S * K * 8
+        comm32 = {"sms": 32, "dispatch_ms": d32, "combine_ms": c32,
+                  "tokens_per_s": R * S / ((d32 + c32) * 1e-3),
+                  "dispatch_gbs": db / (d32 * 1e-3) / 1e9, "combine_gbs": cb / (c32 * 1e-3) / 1e9}
+
     # ---- end to end through the public API with host buffers. Every step uploads its
     # inputs (topk, x, gates, dOut) from pinned host memory and downloads its output.
     # Inputs and outputs are double-buffered on the device and the copies run on a
@@ -326,6 +402,8 @@ def run_gpu(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 12 * args.steps,
         "clocks": clocks,
+        "backward": bwd,
+        "comm_sms_32": comm32,
     }
     return result
 
@@ -465,6 +543,8 @@ def main():
     ap.add_argument("--impl", default="bep", choices=("bep", "reference"))
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the separate timing of the backward GEMMs and dispatch backward")
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_sample:

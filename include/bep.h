@@ -170,6 +170,15 @@ int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const floa
 int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest,
                     const float* gates, int32_t D, uint16_t* dy, void* stream);
 
+/* Gradient of the combine with respect to the gates (the other half of the
+ * combine's backward, [P4] "The core idea"):
+ *   dgates[r,t,k] = sum_c float(dout[r,t,c]) * float(y[dest[r,t,k], c])   (fp32)
+ *   dout [R, S, D] bf16; y [R*S*K, D] bf16 (the combine's input); dest [R, S, K];
+ *   dgates [R, S, K] fp32 out. D % 8 == 0. The fp32 sum's order is the
+ *   library's (per-lane partial sums, then a butterfly over 32 lanes). */
+int bep_combine_dgates(bep_ctx* ctx, const uint16_t* dout, const uint16_t* y, const int32_t* dest,
+                       int32_t D, float* dgates, void* stream);
+
 /* Backward of the dispatch ([P4] "The core idea": in the backward pass the
  * gradients flow back to where the tokens came from): every token's gradient
  * is the sum of the gradients of its K receive rows,
@@ -213,6 +222,14 @@ int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
  *   red [R, B, H, H'] fp32 (in/out: consumed slots become zero). */
 int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, float* red,
                     void* stream);
+
+/* SM budget of the token-moving kernels (dispatch, combine, combine_bwd,
+ * combine_dgates, dispatch_bwd): their grids are sized for `sms` SMs, so
+ * the rest of the GPU stays free for concurrent work, as a communication
+ * library with a fixed SM budget runs ([P4] "Benchmarks against DeepEP v2":
+ * the pages' comparison uses 32 SMs). 0 (the default) = every SM. Affects
+ * only launches made after the call. */
+int bep_set_comm_sms(bep_ctx* ctx, int32_t sms);
 
 /* Waits for `stream`, then reads the status word into *device_err (0 = no
  * device error). The only call that blocks the host. */

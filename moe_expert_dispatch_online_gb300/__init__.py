@@ -37,8 +37,9 @@ BEP_INFER = 1
 # every entry point declared in include/bep.h
 SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_prefetch_weight",
            "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd",
-           "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw", "bep_reduce_grad",
-           "bep_status", "bep_clear_status", "bep_strerror")
+           "bep_combine_dgates", "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw",
+           "bep_reduce_grad", "bep_set_comm_sms", "bep_status", "bep_clear_status",
+           "bep_strerror")
 
 _lib = None
 _lock = threading.Lock()
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH):
             "bep_grouped_gemm": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_combine": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
             "bep_combine_bwd": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
+            "bep_combine_dgates": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
+            "bep_set_comm_sms": (ctypes.c_int, [vp, i32]),
             "bep_dispatch_bwd": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_grouped_gemm_dx": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_grouped_gemm_dw": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
@@ -290,6 +293,22 @@ def bep_combine_bwd(ctx: Context, dout, dest, gates, dy, stream=None):
     _check(load().bep_combine_bwd(ctx.handle, _ptr(dout, _bf16(), "dout"),
                                   _ptr(dest, _i32(), "dest"), _ptr(gates, _f32(), "gates"), D,
                                   _ptr(dy, _bf16(), "dy"), _stream(stream)), "bep_combine_bwd")
+
+
+def bep_combine_dgates(ctx: Context, dout, y, dest, dgates, stream=None):
+    c = ctx.cfg
+    D = int(dout.shape[-1])
+    _numel(dout, c.R * c.S * D, "dout")
+    _numel(y, c.R * c.C * D, "y")
+    _numel(dest, c.R * c.S * c.K, "dest")
+    _numel(dgates, c.R * c.S * c.K, "dgates")
+    _check(load().bep_combine_dgates(ctx.handle, _ptr(dout, _bf16(), "dout"), _ptr(y, _bf16(), "y"),
+                                     _ptr(dest, _i32(), "dest"), D, _ptr(dgates, _f32(), "dgates"),
+                                     _stream(stream)), "bep_combine_dgates")
+
+
+def bep_set_comm_sms(ctx: Context, sms: int):
+    _check(load().bep_set_comm_sms(ctx.handle, int(sms)), "bep_set_comm_sms")
 
 
 def bep_dispatch_bwd(ctx: Context, drecv, dest, dx, stream=None):

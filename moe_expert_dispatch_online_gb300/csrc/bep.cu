@@ -11,6 +11,7 @@ struct bep_ctx {
     void* blob;
     int device;
     int num_sms;
+    int comm_sms;   // SM budget of the token-moving kernels (0: every SM)
 };
 
 namespace {
@@ -60,6 +61,11 @@ T* carve(char*& p, size_t n) {
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BEP_OK : BEP_ERR_CUDA; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// SMs that dispatch, combine and their backward kernels size their grids for.
+int comm_sms(const bep_ctx* ctx) {
+    return (ctx->comm_sms > 0 && ctx->comm_sms < ctx->num_sms) ? ctx->comm_sms : ctx->num_sms;
+}
 
 }  // namespace
 
@@ -132,6 +138,7 @@ int bep_create(const bep_config* cfg, bep_ctx** out) {
     ctx->blob = blob;
     ctx->device = dev;
     ctx->num_sms = sms;
+    ctx->comm_sms = 0;
     *out = ctx;
     return BEP_OK;
 }
@@ -171,7 +178,7 @@ int bep_dispatch(bep_ctx* ctx, const uint16_t* x, const int32_t* dest, uint16_t*
     if (ctx->d.C == 0) return BEP_OK;
     if (!x || !dest || !recv) return BEP_ERR_ARG;
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(dest, 4)) return BEP_ERR_ALIGN;
-    return cuda_rc(bep::launch_dispatch(ctx->d, ctx->ws, x, dest, recv, ctx->num_sms,
+    return cuda_rc(bep::launch_dispatch(ctx->d, ctx->ws, x, dest, recv, comm_sms(ctx),
                                         as_stream(stream)));
 }
 
@@ -195,7 +202,7 @@ int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const floa
     if (!y || !dest || !gates || !out) return BEP_ERR_ARG;
     if (!aligned(y, 16) || !aligned(out, 16) || !aligned(dest, 4) || !aligned(gates, 4))
         return BEP_ERR_ALIGN;
-    return cuda_rc(bep::launch_combine(ctx->d, ctx->ws, y, dest, gates, D, out, ctx->num_sms,
+    return cuda_rc(bep::launch_combine(ctx->d, ctx->ws, y, dest, gates, D, out, comm_sms(ctx),
                                        as_stream(stream)));
 }
 
@@ -207,7 +214,7 @@ int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest, con
     if (!aligned(dout, 16) || !aligned(dy, 16) || !aligned(dest, 4) || !aligned(gates, 4))
         return BEP_ERR_ALIGN;
     return cuda_rc(bep::launch_combine_bwd(ctx->d, ctx->ws, dout, dest, gates, D, dy,
-                                           ctx->num_sms, as_stream(stream)));
+                                           comm_sms(ctx), as_stream(stream)));
 }
 
 int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, uint16_t* dx,
@@ -216,7 +223,7 @@ int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, u
     if (ctx->d.C == 0) return BEP_OK;
     if (!drecv || !dest || !dx) return BEP_ERR_ARG;
     if (!aligned(drecv, 16) || !aligned(dx, 16) || !aligned(dest, 4)) return BEP_ERR_ALIGN;
-    return cuda_rc(bep::launch_dispatch_bwd(ctx->d, ctx->ws, drecv, dest, dx, ctx->num_sms,
+    return cuda_rc(bep::launch_dispatch_bwd(ctx->d, ctx->ws, drecv, dest, dx, comm_sms(ctx),
                                             as_stream(stream)));
 }
 
@@ -257,6 +264,23 @@ int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, flo
         return BEP_ERR_ALIGN;
     return cuda_rc(bep::launch_reduce_grad(ctx->d, ctx->ws, slot_expert, g_home, red,
                                            ctx->num_sms, as_stream(stream)));
+}
+
+int bep_combine_dgates(bep_ctx* ctx, const uint16_t* dout, const uint16_t* y, const int32_t* dest,
+                       int32_t D, float* dgates, void* stream) {
+    if (!ctx || D < 8 || D % 8 != 0) return BEP_ERR_ARG;
+    if (ctx->d.C == 0) return BEP_OK;
+    if (!dout || !y || !dest || !dgates) return BEP_ERR_ARG;
+    if (!aligned(dout, 16) || !aligned(y, 16) || !aligned(dest, 4) || !aligned(dgates, 4))
+        return BEP_ERR_ALIGN;
+    return cuda_rc(bep::launch_combine_dgates(ctx->d, ctx->ws, dout, y, dest, D, dgates,
+                                              comm_sms(ctx), as_stream(stream)));
+}
+
+int bep_set_comm_sms(bep_ctx* ctx, int32_t sms) {
+    if (!ctx || sms < 0) return BEP_ERR_ARG;
+    ctx->comm_sms = sms;
+    return BEP_OK;
 }
 
 int bep_status(bep_ctx* ctx, int32_t* device_err, void* stream) {

@@ -74,6 +74,9 @@ cudaError_t launch_combine(const Dims& d, const Workspace& ws, const uint16_t* y
 cudaError_t launch_combine_bwd(const Dims& d, const Workspace& ws, const uint16_t* dout,
                                const int32_t* dest, const float* gates, int D, uint16_t* dy,
                                int num_sms, cudaStream_t st);
+cudaError_t launch_combine_dgates(const Dims& d, const Workspace& ws, const uint16_t* dout,
+                                  const uint16_t* y, const int32_t* dest, int D, float* dg,
+                                  int num_sms, cudaStream_t st);
 cudaError_t launch_dispatch_bwd(const Dims& d, const Workspace& ws, const uint16_t* drecv,
                                 const int32_t* dest, uint16_t* dx, int num_sms, cudaStream_t st);
 cudaError_t launch_reduce_grad(const Dims& d, const Workspace& ws, const int32_t* slot_expert,

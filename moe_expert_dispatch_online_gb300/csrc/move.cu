@@ -232,6 +232,53 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
     }
 }
 
+// ----------------------------------------------------------------------------- gate gradient
+// dg[tok, k] = sum_c dout[tok, c] * y[dest[tok,k], c] in fp32: each lane sums its
+// columns (16-byte vectors lane, lane+32, ...), then a butterfly reduces the warp.
+__global__ void __launch_bounds__(kThreads) combine_dgates_kernel(const uint4* __restrict__ dout,
+                                                                  const uint4* __restrict__ y,
+                                                                  const int32_t* __restrict__ dest,
+                                                                  float* __restrict__ dg,
+                                                                  int64_t ntok, int K, int nvec,
+                                                                  int64_t nrows, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t tok = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < ntok;
+         tok += nwarps) {
+        unsigned okmask;
+        const int dl = load_dest(dest, tok, K, nrows, &okmask, status);
+        const uint4* src = dout + tok * nvec;
+        for (int k = 0; k < K; ++k) {
+            const int dk = __shfl_sync(0xffffffffu, dl, k);
+            const bool ok = (okmask >> k) & 1u;
+            float acc = 0.0f;
+            if (ok) {
+                const uint4* yr = y + (int64_t)dk * nvec;
+                for (int v0 = 0; v0 < nvec; v0 += 128) {
+                    uint4 a[4], b[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int v = v0 + u * 32 + lane;
+                        a[u] = v < nvec ? src[v] : make_uint4(0, 0, 0, 0);
+                        b[u] = v < nvec ? ld_stream(yr + v) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float fa[8], fb[8];
+                        bf16x8_to_f32(a[u], fa);
+                        bf16x8_to_f32(b[u], fb);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc = __fmaf_rn(fa[i], fb[i], acc);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) dg[tok * K + k] = ok ? acc : 0.0f;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------- prefetch
 // w_slots[s] = w_home[slot_expert[s]] for every used slot s = u*B + j. Each slot is
 // one contiguous [H, H'] block; CTAs stride over 32 KB tiles of it, slot after slot.
@@ -410,6 +457,17 @@ cudaError_t launch_combine(const Dims& d, const Workspace& ws, const uint16_t* y
     if (ntok == 0) return cudaSuccess;
     combine_kernel<4, true><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(y), dest, gates, reinterpret_cast<uint4*>(out), ntok, d.K,
+        D / 8, (int64_t)d.R * d.C, ws.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_dgates(const Dims& d, const Workspace& ws, const uint16_t* dout,
+                                  const uint16_t* y, const int32_t* dest, int D, float* dg,
+                                  int num_sms, cudaStream_t st) {
+    const int64_t ntok = (int64_t)d.R * d.S;
+    if (ntok == 0) return cudaSuccess;
+    combine_dgates_kernel<<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), dest, dg, ntok, d.K,
         D / 8, (int64_t)d.R * d.C, ws.status);
     return cudaGetLastError();
 }
