@@ -43,9 +43,9 @@
 namespace bep {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBChunkBytes = 64 * kBK * 2;      // 8 KB: 64 rows x 64 columns of bf16
+constexpr int kOutBox = 32 * 32 * 4;            // DW epilogue: 32 rows x 32 fp32 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2 };
@@ -56,6 +56,8 @@ struct ModeCfg {
     static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
     static constexpr bool kFix = MODE == kDw;          // tail-zeroing warp
     static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
+    static constexpr int kStages = 4;
+    static constexpr int kOutBufs = MODE == kDw ? 1 : 0;   // fp32 staging boxes per epilogue warp
     static constexpr int kWarps = 2 + kEpiWarps + (kFix ? 1 : 0);
     static constexpr int kThreads = 32 * kWarps;
 };
@@ -122,6 +124,26 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// Element-wise fp32 add of a shared-memory box into global memory, performed by
+// the memory system (one fp32 rounding per element); completion is tracked per
+// issuing thread with bulk groups.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int c0,
+                                                  int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -321,7 +343,8 @@ __device__ __forceinline__ Unit unit_at(const GemmParams& p, int unit, int NT) {
 template <int MODE>
 __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-    const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+    const __grid_constant__ CUtensorMap tmO1, const GemmParams p) {
     using CF = ModeCfg<MODE>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned carve-up: A ring, B ring, barriers
@@ -330,8 +353,10 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     const int BN = p.BN;
     const int b_bytes = BN * kBK * 2;
     uint8_t* smA = smem;
+    constexpr int kStages = CF::kStages;
     uint8_t* smB = smem + kStages * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smB + kStages * b_bytes);
+    uint8_t* smO = smB + kStages * b_bytes;   // DW: a 32x32 fp32 staging box per epilogue warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smO + CF::kEpiWarps * CF::kOutBufs * kOutBox);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* fix = bars + 2 * kStages;
@@ -474,24 +499,30 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             const int row = q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_stride);
             if (MODE == kDw) {
-                float* out = (u.t.wsel >= 0 ? p.g_home + (int64_t)u.t.wsel * p.H * p.N
-                                            : p.red + (int64_t)(-1 - u.t.wsel) * p.H * p.N);
-                float4* orow = reinterpret_cast<float4*>(
-                    out + (int64_t)(u.mblk * kBM + row) * p.N + (int64_t)u.nt * BN);
+                // 32 rows x 32 columns at a time: stage the fp32 box in shared memory
+                // (128-byte swizzle: 16-byte piece j of row r sits at j ^ (r & 7)), then
+                // one lane has the memory system add it to the gradient rows (one fp32
+                // rounding per element). Measured alternatives -- two staging boxes per
+                // warp with a 3-stage operand ring, and per-thread red.global.add.v4 --
+                // were slower on the S=8192, E=384 workload.
+                const CUtensorMap* tmO = u.t.wsel >= 0 ? &tmO0 : &tmO1;
+                const int orow0 = (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel)) * p.H +
+                                  u.mblk * kBM + q * 32;
+                uint8_t* stg = smO + e * kOutBox;
+                uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
                 for (int c0 = c_lo; c0 < c_lo + cspan; c0 += 32) {
-                    float4 old[8];
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) old[v] = orow[c0 / 4 + v];
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                    if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                    __syncwarp();
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float4 o = old[v];
-                        o.x = __fadd_rn(o.x, __uint_as_float(r[4 * v + 0]));
-                        o.y = __fadd_rn(o.y, __uint_as_float(r[4 * v + 1]));
-                        o.z = __fadd_rn(o.z, __uint_as_float(r[4 * v + 2]));
-                        o.w = __fadd_rn(o.w, __uint_as_float(r[4 * v + 3]));
-                        orow[c0 / 4 + v] = o;
+                    for (int j = 0; j < 8; ++j)
+                        srow[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(tmO, stg, u.nt * BN + c0, orow0);
+                        bulk_commit();
                     }
                 }
             } else {
@@ -518,6 +549,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
         }
+        // DW: every reduce this warp issued has been applied before the CTA ends
+        if (MODE == kDw && lane == 0) bulk_wait_all();
+        __syncwarp();
     } else if (CF::kFix) {
         // ---------------------------------------------------- tail fix-up (DW)
         // The last K block of a segment holds rows of the next segment past
@@ -605,14 +639,32 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
     return r == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor [rows, cols], 32 x 32 boxes (128-byte rows), 128-byte swizzle: the
+// target of the DW epilogue's bulk reduce-add.
+bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int pick_bn(int n) {
     for (int bn = 256; bn >= 64; bn -= 64)
         if (n % bn == 0) return bn;
     return 64;
 }
 
+template <int MODE>
 size_t smem_bytes(int BN) {
-    return 1024 + (size_t)kStages * (kABytes + BN * kBK * 2) + (3 * kStages + 4) * 8 + 16;
+    using CF = ModeCfg<MODE>;
+    const size_t stage_out = (size_t)CF::kEpiWarps * CF::kOutBufs * kOutBox;
+    return 1024 + (size_t)CF::kStages * (kABytes + BN * kBK * 2) + stage_out +
+           (3 * CF::kStages + 4) * 8 + 16;
 }
 
 int tmem_cols_for(int BN) {
@@ -623,9 +675,10 @@ int tmem_cols_for(int BN) {
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const GemmParams& prm, int num_sms, cudaStream_t st) {
-    grouped_gemm_kernel<MODE><<<num_sms, ModeCfg<MODE>::kThreads, smem_bytes(prm.BN), st>>>(a, b0, b1,
-                                                                                             prm);
+                        const CUtensorMap& o0, const CUtensorMap& o1, const GemmParams& prm,
+                        int num_sms, cudaStream_t st) {
+    grouped_gemm_kernel<MODE><<<num_sms, ModeCfg<MODE>::kThreads, smem_bytes<MODE>(prm.BN), st>>>(
+        a, b0, b1, o0, o1, prm);
     return cudaGetLastError();
 }
 
@@ -635,12 +688,14 @@ cudaError_t gemm_setup(int device) {
     (void)device;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    const int sm = (int)smem_bytes(256);
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<kFwd>(256));
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<kDx>(256));
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(grouped_gemm_kernel<kDw>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    return cudaFuncSetAttribute(grouped_gemm_kernel<kDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<kDw>(256));
 }
 
 cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -669,7 +724,7 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = 1;
     prm.status = ws.status;
-    return launch_mode<kFwd>(tmA, tmBh, tmBs, prm, num_sms, st);
+    return launch_mode<kFwd>(tmA, tmBh, tmBs, tmA, tmA, prm, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -699,7 +754,7 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = 1;
     prm.status = ws.status;
-    return launch_mode<kDx>(tmA, tmBh, tmBs, prm, num_sms, st);
+    return launch_mode<kDx>(tmA, tmBh, tmBs, tmA, tmA, prm, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -714,6 +769,11 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int
     // A: recv^T in 64 (h) x 64 (row) boxes; B: dY in 64 (h') x 64 (row) boxes
     if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBK, 64)) return cudaErrorInvalidValue;
     if (!encode_2d(&tmB, dy, (uint64_t)d.R * d.C, d.Hp, kBK, 64)) return cudaErrorInvalidValue;
+    // outputs: g_home as [E*H, H'] and red as [R*B*H, H'] fp32 rows
+    CUtensorMap tmG, tmR;
+    if (!encode_2d_f32(&tmG, g_home, (uint64_t)d.E * d.H, d.Hp)) return cudaErrorInvalidValue;
+    const uint64_t red_rows = (uint64_t)(d.R * d.B > 0 ? d.R * d.B : 1) * d.H;
+    if (!encode_2d_f32(&tmR, red, red_rows, d.Hp)) return cudaErrorInvalidValue;
     GemmParams prm = {};
     prm.tiles = ws.tiles;
     prm.ntiles = ws.ntiles;
@@ -726,7 +786,7 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = d.H / kBM;
     prm.status = ws.status;
-    return launch_mode<kDw>(tmA, tmB, tmB, prm, num_sms, st);
+    return launch_mode<kDw>(tmA, tmB, tmB, tmG, tmR, prm, num_sms, st);
 }
 
 }  // namespace bep

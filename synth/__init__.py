@@ -70,6 +70,10 @@ WORKLOADS = {
     # the bench's expert shape (H=7168, H'=2048) on a few GB: profiling captures
     "gemm_probe_r4_e16": Workload("gemm_probe_r4_e16", R=4, S=2048, E=16, K=8, H=7168, Hp=2048,
                                   B=4, mode=MODE_TRAIN),
+    # about 1,700 rows per segment, like the bench-shaped workload's ~1,400: profiling
+    # of the weight-gradient GEMM, whose cost grows with the number of segments
+    "dw_probe_r4_e16_s1024": Workload("dw_probe_r4_e16_s1024", R=4, S=1024, E=16, K=8, H=7168,
+                                      Hp=2048, B=4, mode=MODE_TRAIN),
 }
 
 MAXVIO_TARGETS = {
@@ -79,6 +83,7 @@ MAXVIO_TARGETS = {
     "infer_r8_e384_b4": (1.0, 20.0),
     "grad_r8_e64": (10.0,),
     "gemm_probe_r4_e16": (None,),
+    "dw_probe_r4_e16_s1024": (None,),
 }
 
 
