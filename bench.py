@@ -271,6 +271,41 @@ def run_gpu(args, rank, world, local_rank):
                   "tokens_per_s": R * S / ((d32 + c32) * 1e-3),
                   "dispatch_gbs": db / (d32 * 1e-3) / 1e9, "combine_gbs": cb / (c32 * 1e-3) / 1e9}
 
+    # ---- the VM group GEMM through the weight store's aliased [E+B, H, H'] views
+    vmg = None
+    if not args.no_backward:
+        try:
+            store = bep.WeightStore(cfg, layers=1)
+        except bep.BepError as exc:
+            vmg = {"unavailable": str(exc)}
+            store = None
+        if store is not None:
+            s_home, s_slots, s_views = store.home(0), store.slots(), store.views(0)
+            s_home.copy_(w_home)
+            nb = min(args.steps, 2 * len(topks))
+            vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
+            for i in range(nb + 1):
+                bep.bep_plan(ctx, topks[i % len(topks)], buf.cu_seqlens, buf.slot_expert,
+                             buf.dest, buf.maxvio, stream)
+                bep.bep_prefetch_weight(ctx, buf.slot_expert, s_home, s_slots, stream)
+                bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+                if i > 0:
+                    vev[i - 1][0].record(stream)
+                bep.bep_grouped_gemm_vm(ctx, buf.cu_seqlens, buf.recv, s_views, buf.y, stream)
+                if i > 0:
+                    vev[i - 1][1].record(stream)
+            torch.cuda.synchronize()
+            st = bep.bep_status(ctx, stream)
+            if st:
+                raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+            vm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in vev)
+            fl = 2.0 * R * S * K * H * Hp
+            vmg = {"ms": vm_ms, "tflops": fl / (vm_ms * 1e-3) / 1e12,
+                   "frac_bf16_sustained": fl / (vm_ms * 1e-3) / 1e12 / peaks()["bf16_sus"]}
+            del s_home, s_slots, s_views
+            store.close()
+            torch.cuda.empty_cache()
+
     # ---- end to end through the public API with host buffers. Every step uploads its
     # inputs (topk, x, gates, dOut) from pinned host memory and downloads its output.
     # Inputs and outputs are double-buffered on the device and the copies run on a
@@ -404,6 +439,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "backward": bwd,
         "comm_sms_32": comm32,
+        "vm_group_gemm": vmg,
     }
     return result
 

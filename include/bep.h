@@ -156,6 +156,34 @@ int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* re
                      const uint16_t* w_home, const uint16_t* w_slots, uint16_t* y,
                      void* stream);
 
+/* The pages' "VM group GEMM" ([P4] "The memory contract": each rank's weights
+ * are one contiguous [E+B, H, H'] tensor and the GEMM addresses experts by row
+ * index only): the product of bep_grouped_gemm, with rank u's weight row rho
+ * read from w_views[u][rho].
+ *   w_views [R, E+B, H, H'] bf16: the R per-rank tensors back to back, e.g. the
+ *           aliased views of bep_weights_create (no copy), or any buffer laid
+ *           out that way. */
+int bep_grouped_gemm_vm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                        const uint16_t* w_views, uint16_t* y, void* stream);
+
+/* Weight store with the pages' memory contract ([P4] "The memory contract"):
+ * per layer one physical block of home rows [E, H, H'], one slot pool
+ * [R, B, H, H'] shared by every layer (the extra memory is B experts per
+ * projection in total, not per layer), and per layer R views [E+B, H, H'],
+ * back to back, in which rank u's rows [0, E) alias the layer's home rows and
+ * rows [E, E+B) alias rank u's part of the pool (CUDA virtual memory
+ * management; nothing is copied). E*H*H'*2 and B*H*H'*2 bytes must be
+ * multiples of the mapping granularity (2 MiB), else BEP_ERR_SIZE. The store
+ * allocates device memory; bep_weights_destroy frees it. */
+typedef struct bep_weights bep_weights;
+int bep_weights_create(const bep_config* cfg, int32_t layers, bep_weights** out);
+/* Device pointers of layer `layer`: home [E, H, H'], the shared pool
+ * [R, B, H, H'] (the w_slots of bep_prefetch_weight), views [R, E+B, H, H']
+ * (the w_views of bep_grouped_gemm_vm). Any output pointer may be NULL. */
+int bep_weights_get(bep_weights* w, int32_t layer, uint16_t** home, uint16_t** slots,
+                    uint16_t** views);
+void bep_weights_destroy(bep_weights* w);
+
 /* Weighted unpermute/combine ([P4] "The core idea": fused permute/unpermute):
  *   out[r,t,c] = bf16_rne(acc), acc = 0; for k = 0..K-1:
  *                acc = fmaf(gates[r,t,k], float(y[dest[r,t,k], c]), acc)

@@ -38,8 +38,9 @@ BEP_INFER = 1
 SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_prefetch_weight",
            "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd",
            "bep_combine_dgates", "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw",
-           "bep_reduce_grad", "bep_set_comm_sms", "bep_status", "bep_clear_status",
-           "bep_strerror")
+           "bep_grouped_gemm_vm", "bep_weights_create", "bep_weights_get",
+           "bep_weights_destroy", "bep_reduce_grad", "bep_set_comm_sms", "bep_status",
+           "bep_clear_status", "bep_strerror")
 
 _lib = None
 _lock = threading.Lock()
@@ -75,6 +76,12 @@ def load(path: str = LIB_PATH):
             "bep_grouped_gemm": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_combine": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
             "bep_combine_bwd": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
+            "bep_grouped_gemm_vm": (ctypes.c_int, [vp, p, p, p, p, vp]),
+            "bep_weights_create": (ctypes.c_int, [ctypes.POINTER(_Config), i32,
+                                                  ctypes.POINTER(vp)]),
+            "bep_weights_get": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                               ctypes.POINTER(vp)]),
+            "bep_weights_destroy": (None, [vp]),
             "bep_combine_dgates": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
             "bep_set_comm_sms": (ctypes.c_int, [vp, i32]),
             "bep_dispatch_bwd": (ctypes.c_int, [vp, p, p, p, vp]),
@@ -293,6 +300,76 @@ def bep_combine_bwd(ctx: Context, dout, dest, gates, dy, stream=None):
     _check(load().bep_combine_bwd(ctx.handle, _ptr(dout, _bf16(), "dout"),
                                   _ptr(dest, _i32(), "dest"), _ptr(gates, _f32(), "gates"), D,
                                   _ptr(dy, _bf16(), "dy"), _stream(stream)), "bep_combine_bwd")
+
+
+def bep_grouped_gemm_vm(ctx: Context, cu_seqlens, recv, w_views, y, stream=None):
+    """The grouped GEMM with each rank's weights as one [E+B, H, H'] tensor: w_views
+    is [R, E+B, H, H'] (a WeightStore view or any tensor laid out that way)."""
+    c = ctx.cfg
+    _numel(cu_seqlens, c.R * (c.E + c.B + 1), "cu_seqlens")
+    _numel(recv, c.R * c.C * c.H, "recv")
+    _numel(w_views, c.R * (c.E + c.B) * c.H * c.Hp, "w_views")
+    _numel(y, c.R * c.C * c.Hp, "y")
+    _check(load().bep_grouped_gemm_vm(ctx.handle, _ptr(cu_seqlens, _i32(), "cu_seqlens"),
+                                      _ptr(recv, _bf16(), "recv"),
+                                      _ptr(w_views, _bf16(), "w_views"), _ptr(y, _bf16(), "y"),
+                                      _stream(stream)), "bep_grouped_gemm_vm")
+
+
+class WeightStore:
+    """bep_weights: per layer home rows [E, H, H'], one prefetch-slot pool [R, B, H, H']
+    shared by all layers, and per layer R aliased [E+B, H, H'] views (no copies).
+    Tensors returned by home()/slots()/views() alias device memory the store owns:
+    keep the store alive while they are used."""
+
+    def __init__(self, cfg: Config, layers: int = 1):
+        lib = load()
+        c = _Config(cfg.R, cfg.E, cfg.B, cfg.K, cfg.S, cfg.H, cfg.Hp, cfg.mode)
+        h = ctypes.c_void_p()
+        _check(lib.bep_weights_create(ctypes.byref(c), int(layers), ctypes.byref(h)),
+               "bep_weights_create")
+        self.cfg, self.layers, self.handle = cfg, layers, h
+
+    def _ptrs(self, layer):
+        home, slots, views = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        _check(load().bep_weights_get(self.handle, int(layer), ctypes.byref(home),
+                                      ctypes.byref(slots), ctypes.byref(views)),
+               "bep_weights_get")
+        return home.value, slots.value, views.value
+
+    def _tensor(self, addr, shape):
+        import torch
+        n = 1
+        for s_ in shape:
+            n *= s_
+        # zero-copy view of device memory the store owns, through the CUDA array interface
+        class _Arr:
+            __cuda_array_interface__ = {"shape": (n,), "typestr": "<i2", "data": (addr, False),
+                                        "version": 3, "strides": None}
+        return torch.as_tensor(_Arr(), device="cuda").view(torch.bfloat16).view(*shape)
+
+    def home(self, layer):
+        c = self.cfg
+        return self._tensor(self._ptrs(layer)[0], (c.E, c.H, c.Hp))
+
+    def slots(self):
+        c = self.cfg
+        return self._tensor(self._ptrs(0)[1], (c.R, c.B, c.H, c.Hp))
+
+    def views(self, layer):
+        c = self.cfg
+        return self._tensor(self._ptrs(layer)[2], (c.R, c.E + c.B, c.H, c.Hp))
+
+    def close(self):
+        if self.handle:
+            load().bep_weights_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def bep_combine_dgates(ctx: Context, dout, y, dest, dgates, stream=None):

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbep.so")
-SOURCES = ["bep.cu", "plan.cu", "move.cu", "gemm.cu"]
+SOURCES = ["bep.cu", "plan.cu", "move.cu", "gemm.cu", "vmm.cu"]
 HEADERS = ["bep_internal.cuh", os.path.join("..", "..", "include", "bep.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

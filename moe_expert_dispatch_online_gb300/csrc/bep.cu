@@ -195,6 +195,17 @@ int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* re
                                             y, ctx->num_sms, as_stream(stream)));
 }
 
+int bep_grouped_gemm_vm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                        const uint16_t* w_views, uint16_t* y, void* stream) {
+    if (!ctx) return BEP_ERR_ARG;
+    if (ctx->d.C == 0) return BEP_OK;
+    if (!cu_seqlens || !recv || !w_views || !y) return BEP_ERR_ARG;
+    if (!aligned(cu_seqlens, 4) || !aligned(recv, 16) || !aligned(w_views, 16) || !aligned(y, 16))
+        return BEP_ERR_ALIGN;
+    return cuda_rc(bep::launch_grouped_gemm_vm(ctx->d, ctx->ws, cu_seqlens, recv, w_views, y,
+                                               ctx->num_sms, as_stream(stream)));
+}
+
 int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const float* gates,
                 int32_t D, uint16_t* out, void* stream) {
     if (!ctx || D < 8 || D % 8 != 0) return BEP_ERR_ARG;

@@ -87,6 +87,9 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
                                 const uint16_t* recv, const uint16_t* w_home,
                                 const uint16_t* w_slots, uint16_t* y, int num_sms,
                                 cudaStream_t st);
+cudaError_t launch_grouped_gemm_vm(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* recv, const uint16_t* w_views, uint16_t* y,
+                                   int num_sms, cudaStream_t st);
 cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
                                    const uint16_t* dy, const uint16_t* w_home,
                                    const uint16_t* w_slots, uint16_t* drecv, int num_sms,

@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             t.row0 = (int32_t)(u * d.C + s + m * kBM);
             t.rows = seg_mode ? l : min(kBM, l - m * kBM);
             t.wsel = wsel;
-            t.pad = 0;
+            t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
             ws.tiles[run + m] = t;
         }
         run += n;
@@ -304,6 +304,7 @@ struct GemmParams {
     int BN;
     int tmem_cols;
     int mtd;             // DW: m-blocks per weight row (H / 128)
+    int vm;              // FWD / DX: weights as R consecutive [E+B, H, H'] views (tmB0)
     int32_t* status;
 };
 
@@ -406,8 +407,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
                 const int n0 = u.nt * BN;
-                const CUtensorMap* tmB = (MODE == kDw || u.t.wsel >= 0) ? &tmB0 : &tmB1;
-                const int brow0 = (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel)) * p.H;
+                const CUtensorMap* tmB = (MODE == kDw || p.vm || u.t.wsel >= 0) ? &tmB0 : &tmB1;
+                const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
@@ -725,6 +726,37 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     prm.mtd = 1;
     prm.status = ws.status;
     return launch_mode<kFwd>(tmA, tmBh, tmBs, tmA, tmA, prm, num_sms, st);
+}
+
+// The pages' "VM group GEMM": every rank's weights are one contiguous [E+B, H, H']
+// tensor and the GEMM addresses them by row index alone. w_views holds the R
+// views back to back ([R, E+B, H, H']); with bep_weights_create they alias the
+// home rows and the shared slot pool without copies.
+cudaError_t launch_grouped_gemm_vm(const Dims& d, const Workspace& ws, const int32_t* cu,
+                                   const uint16_t* recv, const uint16_t* w_views, uint16_t* y,
+                                   int num_sms, cudaStream_t st) {
+    if (d.C == 0) return cudaSuccess;
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
+    const int BN = pick_bn(d.Hp);
+    CUtensorMap tmA, tmV;
+    if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBM, kBK)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tmV, w_views, (uint64_t)d.R * d.NROW * d.H, d.Hp, kBK, 64))
+        return cudaErrorInvalidValue;
+    GemmParams prm = {};
+    prm.tiles = ws.tiles;
+    prm.ntiles = ws.ntiles;
+    prm.out = y;
+    prm.N = d.Hp;
+    prm.Kdim = d.H;
+    prm.H = d.H;
+    prm.BN = BN;
+    prm.tmem_cols = tmem_cols_for(BN);
+    prm.mtd = 1;
+    prm.vm = 1;
+    prm.status = ws.status;
+    return launch_mode<kFwd>(tmA, tmV, tmV, tmA, tmA, prm, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
