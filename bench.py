@@ -446,93 +446,114 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def cpu_sample(seconds_hint: float = 1.0):
-    """Times the oracle, as it stands, on a bounded sample of the bench workload and
-    scales each stage's cost to one whole step. Runs single-threaded (BLAS threads 1)."""
-    import numpy as np
+class CpuSample:
+    """The oracle, as it stands, on a bounded sample of the bench workload; each
+    stage's cost is scaled to one whole step. Inputs are drawn once; step() times
+    the oracle's work only. Runs single-threaded (BLAS threads pinned to 1)."""
 
-    import oracle
-    import synth
+    N_TOK = 256      # tokens in the dispatch / combine sample
+    M_ROWS = 64      # receive rows in the GEMM sample
+    FRAC = 16        # prefetch / reduce_grad run on 1/FRAC of one slot
 
-    wl = synth.WORKLOADS[WORKLOAD]
-    R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
-    C = S * K
-    topk = synth.routing(wl, 10.0, 0)
-    t0 = time.perf_counter()
-    p = oracle.plan(topk, E, B, wl.mode)
-    t_plan = time.perf_counter() - t0
-    n = 256                                             # tokens in the data sample
-    x = synth.tokens_host((1, n, H), 1)
-    dest = np.arange(n * K, dtype=np.int32).reshape(1, n, K)
-    g = synth.gates_host(1, n, K, 1)
-    t0 = time.perf_counter()
-    recv = oracle.dispatch(x, dest)
-    t_disp = (time.perf_counter() - t0) * (R * S / n)
-    y = synth.tokens_host((n * K, Hp), 2)
-    t0 = time.perf_counter()
-    oracle.combine(y, dest, g)
-    t_comb = (time.perf_counter() - t0) * (R * S / n)
-    dout = synth.tokens_host((1, n, Hp), 3)
-    t0 = time.perf_counter()
-    oracle.combine_bwd(dout, dest, g)
-    t_bwd = (time.perf_counter() - t0) * (R * S / n)
-    w = synth.weights_host((H, Hp), 4)
-    m = 64                                              # GEMM rows in the sample
-    t0 = time.perf_counter()
-    oracle.gemm_rows(recv[:m], w)
-    t_gemm_rows = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.bf16_to_f32(w).astype(np.float64)
-    t_wconv = time.perf_counter() - t0
-    nseg = int(sum((np.diff(p.cu[u]) > 0).sum() for u in range(R)))
-    t_gemm = (t_gemm_rows - t_wconv) * (R * C / m) + t_wconv * nseg
-    used = int((p.slot_expert >= 0).sum())
-    gsz = (H * Hp) // 16                                # 1/16 of one slot
-    G1 = np.zeros((1, gsz), np.float32)
-    red1 = np.ones((1, 1, gsz), np.float32)
-    t0 = time.perf_counter()
-    oracle.reduce_grad(G1, red1, np.zeros((1, 1), np.int32))
-    t_red = (time.perf_counter() - t0) * 16 * used
-    w_home = synth.weights_host((1, H * Hp // 16), 5)
-    slots = np.zeros((1, 1, H * Hp // 16), np.uint16)
-    t0 = time.perf_counter()
-    oracle.prefetch(w_home, np.zeros((1, 1), np.int32), slots)
-    t_pref = (time.perf_counter() - t0) * 16 * used
-    step_s = t_plan + t_pref + t_disp + t_gemm + t_comb + t_bwd + t_red
-    return {
-        "value": R * S / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-        "sample": (f"maxvio-10 routing: plan on all {R * S} tokens; dispatch/combine/combine_bwd on "
-                   f"{n} tokens; GEMM on {m} rows + one weight conversion (scaled by {nseg} "
-                   f"segments); prefetch/reduce_grad on 1/16 slot (scaled by {used} slots); "
-                   f"scaled to one step of {R * S} tokens"),
-        "step_seconds_est": step_s,
-        "stages_s": {"plan": t_plan, "prefetch": t_pref, "dispatch": t_disp, "gemm": t_gemm,
-                     "combine": t_comb, "combine_bwd": t_bwd, "reduce_grad": t_red},
-    }
+    def __init__(self):
+        import numpy as np
+
+        import synth
+        self.np = np
+        wl = synth.WORKLOADS[WORKLOAD]
+        self.wl = wl
+        R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+        n = self.N_TOK
+        self.topk = synth.routing(wl, 10.0, 0)
+        self.x = synth.tokens_host((1, n, H), 1)
+        self.dest = np.arange(n * K, dtype=np.int32).reshape(1, n, K)
+        self.g = synth.gates_host(1, n, K, 1)
+        self.y = synth.tokens_host((n * K, Hp), 2)
+        self.dout = synth.tokens_host((1, n, Hp), 3)
+        self.w = synth.weights_host((H, Hp), 4)
+        gsz = (H * Hp) // self.FRAC
+        self.G1 = np.zeros((1, gsz), np.float32)
+        self.red1 = np.ones((1, 1, gsz), np.float32)
+        self.w_home1 = synth.weights_host((1, gsz), 5)
+        self.slots1 = np.zeros((1, 1, gsz), np.uint16)
+        self.zero_map = np.zeros((1, 1), np.int32)
+
+    def step(self):
+        import oracle
+        np = self.np
+        wl = self.wl
+        R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+        C, n, m = S * K, self.N_TOK, self.M_ROWS
+        tok_scale = R * S / n
+        t0 = time.perf_counter()
+        p = oracle.plan(self.topk, E, B, wl.mode)
+        t_plan = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        recv = oracle.dispatch(self.x, self.dest)
+        t_disp = (time.perf_counter() - t0) * tok_scale
+        t0 = time.perf_counter()
+        oracle.combine(self.y, self.dest, self.g)
+        t_comb = (time.perf_counter() - t0) * tok_scale
+        t0 = time.perf_counter()
+        oracle.combine_bwd(self.dout, self.dest, self.g)
+        t_bwd = (time.perf_counter() - t0) * tok_scale
+        t0 = time.perf_counter()
+        oracle.gemm_rows(recv[:m], self.w)
+        t_gemm_rows = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.bf16_to_f32(self.w).astype(np.float64)
+        t_wconv = time.perf_counter() - t0
+        nseg = int(sum((np.diff(p.cu[u]) > 0).sum() for u in range(R)))
+        t_gemm = max(t_gemm_rows - t_wconv, 0.0) * (R * C / m) + t_wconv * nseg
+        used = int((p.slot_expert >= 0).sum())
+        t0 = time.perf_counter()
+        oracle.reduce_grad(self.G1, self.red1, self.zero_map)
+        t_red = (time.perf_counter() - t0) * self.FRAC * used
+        t0 = time.perf_counter()
+        oracle.prefetch(self.w_home1, self.zero_map, self.slots1)
+        t_pref = (time.perf_counter() - t0) * self.FRAC * used
+        step_s = t_plan + t_pref + t_disp + t_gemm + t_comb + t_bwd + t_red
+        return {
+            "value": R * S / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"maxvio-10 routing: plan on all {R * S} tokens; dispatch/combine/"
+                       f"combine_bwd on {n} tokens; GEMM on {m} rows + one weight conversion "
+                       f"(scaled by {nseg} segments); prefetch/reduce_grad on 1/{self.FRAC} slot "
+                       f"(scaled by {used} slots); scaled to one step of {R * S} tokens"),
+            "step_seconds_est": step_s,
+            "stages_s": {"plan": t_plan, "prefetch": t_pref, "dispatch": t_disp, "gemm": t_gemm,
+                         "combine": t_comb, "combine_bwd": t_bwd, "reduce_grad": t_red},
+        }
 
 
-def cpu_baseline_subprocess():
+def cpu_samples(steps: int, warmup: int):
+    cs = CpuSample()
+    out = []
+    for i in range(warmup + steps):
+        r = cs.step()
+        if i >= warmup:
+            out.append(r)
+    return out
+
+
+def cpu_baseline_subprocess(steps: int = 1, warmup: int = 0):
+    """The oracle timing in a fresh single-threaded process (BLAS threads 1)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample"], env=env,
-                       capture_output=True, text=True, timeout=900)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample",
+                        "--steps", str(steps), "--warmup", str(warmup)], env=env,
+                       capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
-        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+        return [{"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}]
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle on the host cores, each step one bounded sample."""
     if rank != 0:
         return None
-    times = []
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        res = cpu_baseline_subprocess()
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(res)
-    vals = [r["value"] for r in times if "value" in r]
+    res = cpu_baseline_subprocess(args.steps, args.warmup)
+    vals = [r["value"] for r in res if "value" in r]
     v = statistics.mean(vals) if vals else None
-    base = times[-1] if times else {}
+    base = res[-1] if res else {}
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -541,6 +562,7 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{WORKLOAD} (R=8, S=8192/rank, E=384, K=8, H=7168, H'=2048, B=48)"},
         "cpu_baseline": {k: base.get(k) for k in ("kind", "cores", "sample")} | {"value": v},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        **({"error": base["error"]} if "error" in base else {}),
     }
 
 
@@ -585,7 +607,7 @@ def main():
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_sample:
-        print(json.dumps(cpu_sample()))
+        print(json.dumps(cpu_samples(args.steps, args.warmup)))
         return
     rank, world, local = dist_init()
     if args.impl == "reference":
@@ -596,7 +618,7 @@ def main():
     res = run_gpu(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess().items()
+            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess()[0].items()
                                    if k in ("value", "unit", "cores", "kind", "sample", "error")}
         print(json.dumps(res))
 
