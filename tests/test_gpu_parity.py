@@ -477,3 +477,58 @@ def test_forward_and_backward_fold_in_one_stream_graph(lib):
         assert np.linalg.norm(out - out_ref) / np.linalg.norm(out_ref) <= GEMM_RTOL
         np.testing.assert_array_equal(host_u16(buf.dy), oracle.combine_bwd(dout_h, ref.dest, gates_h))
     assert bep.bep_status(ctx) == 0
+
+
+@pytest.mark.parametrize("R,S,K,E,B,mode,H,Hp", [
+    (2, 100, 2, 8, 4, 0, 192, 192),     # BN = 192 (forward and dX), ragged segments
+    (2, 300, 4, 16, 8, 0, 384, 128),    # BN = 128
+    (4, 200, 4, 32, 1, 1, 256, 320),    # inference, overflow rows, BN = 64
+])
+def test_grouped_gemm_tile_shapes(lib, R, S, K, E, B, mode, H, Hp):
+    """Forward and input-gradient GEMMs in full on shapes that select each N tile
+    width, against binary64 per segment."""
+    bep = lib
+    topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 1.4), 11)
+    if mode == 1:   # every token on home group 0: ranks need more remote experts than B
+        pop = np.full(E, 1e-12)
+        pop[:E // R] = 1.0
+        topk = synth.gumbel_topk(R, S, K, pop / pop.sum(), 12)
+    ref = oracle.plan(topk, E, B, mode)
+    cfg = bep.Config(R=R, E=E, B=B, K=K, S=S, H=H, Hp=Hp, mode=mode)
+    ctx, buf = gpu_plan(bep, cfg, topk)
+    assert_plan_equal(buf, ref)
+    x = synth.tokens_host((R, S, H), 21)
+    w_home = synth.weights_host((E, H, Hp), 22)
+    dy = synth.tokens_host((R * S * K, Hp), 23)
+    recv_ref = oracle.dispatch(x, ref.dest)
+    slots_ref = oracle.prefetch(w_home, ref.slot_expert, np.zeros((R, B, H, Hp), np.uint16))
+    y_ref = oracle.grouped_gemm(recv_ref, w_home, slots_ref, ref.cu, E)
+    dr_ref = oracle.grouped_gemm_dx(dy, w_home, slots_ref, ref.cu, E)
+    w_home_d = dev_u16(w_home)
+    w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home_d, w_slots)
+    bep.bep_dispatch(ctx, dev_u16(x), buf.dest, buf.recv)
+    gy = Guarded((R * S * K, Hp), torch.bfloat16)
+    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home_d, w_slots, gy.t)
+    gd = Guarded((R * S * K, H), torch.bfloat16)
+    bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, dev_u16(dy), w_home_d, w_slots, gd.t)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    assert gy.intact() and gd.intact()
+    y = oracle.bf16_to_f32(host_u16(gy.t)).astype(np.float64)
+    dr = oracle.bf16_to_f32(host_u16(gd.t)).astype(np.float64)
+    C = S * K
+    nseg = 0
+    for u in range(R):
+        for rho in range(E + B):
+            a, b = ref.cu[u, rho], ref.cu[u, rho + 1]
+            if b == a:
+                continue
+            nseg += 1
+            for got, want in ((y, y_ref), (dr, dr_ref)):
+                g_, w_ = got[u * C + a:u * C + b], want[u * C + a:u * C + b]
+                assert np.linalg.norm(g_ - w_) / max(np.linalg.norm(w_), 1e-30) <= GEMM_RTOL, (u, rho)
+    if mode == 1:
+        G = E // R
+        assert any(ref.cu[u, e + 1] > ref.cu[u, e] for u in range(R) for e in range(E)
+                   if e // G != u), "the case must exercise overflow rows"
