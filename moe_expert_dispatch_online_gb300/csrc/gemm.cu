@@ -504,8 +504,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 // (128-byte swizzle: 16-byte piece j of row r sits at j ^ (r & 7)), then
                 // one lane has the memory system add it to the gradient rows (one fp32
                 // rounding per element). Measured alternatives -- two staging boxes per
-                // warp with a 3-stage operand ring, and per-thread red.global.add.v4 --
-                // were slower on the S=8192, E=384 workload.
+                // warp with a 3-stage operand ring, per-thread red.global.add.v4, and a
+                // load/add/store on the LSU path with the next chunk in flight -- were
+                // slower on the S=8192, E=384 workload.
                 const CUtensorMap* tmO = u.t.wsel >= 0 ? &tmO0 : &tmO1;
                 const int orow0 = (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel)) * p.H +
                                   u.mblk * kBM + q * 32;
