@@ -151,7 +151,9 @@ int bep_dispatch(bep_ctx* ctx, const uint16_t* x, const int32_t* dest, uint16_t*
  *   y[u*S*K + seg, :] = recv[u*S*K + seg, :] @ W(u, rho),
  *   W(u, rho) = rho < E ? w_home[rho] : w_slots[u][rho - E]   ([H, H'] bf16),
  * bf16 inputs, fp32 accumulation, bf16 (round to nearest even) output.
- * Rows of y outside every segment are not written. */
+ * Rows of y outside every segment are not written. A cu_seqlens table with any
+ * segment outside [0, S*K] or ending before it starts is refused as a whole
+ * (BEP_DERR_BOUNDS, nothing written); the same holds for the other GEMMs. */
 int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
                      const uint16_t* w_home, const uint16_t* w_slots, uint16_t* y,
                      void* stream);
@@ -258,6 +260,13 @@ int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, flo
  * the pages' comparison uses 32 SMs). 0 (the default) = every SM. Affects
  * only launches made after the call. */
 int bep_set_comm_sms(bep_ctx* ctx, int32_t sms);
+
+/* Failure-path self-test (the pages have no counterpart): one GPU thread waits,
+ * through the same bounded-wait code the grouped GEMMs use, on a barrier that
+ * nothing ever signals. After timeout_us (1 .. 10^7) the wait gives up, sets
+ * BEP_DERR_TIMEOUT in the status word and the kernel returns, so the context
+ * stays usable. Asynchronous on `stream`. */
+int bep_wait_selftest(bep_ctx* ctx, int32_t timeout_us, void* stream);
 
 /* Waits for `stream`, then reads the status word into *device_err (0 = no
  * device error). The only call that blocks the host. */

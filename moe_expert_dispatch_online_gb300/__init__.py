@@ -39,8 +39,8 @@ SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_pre
            "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd",
            "bep_combine_dgates", "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw",
            "bep_grouped_gemm_vm", "bep_weights_create", "bep_weights_get",
-           "bep_weights_destroy", "bep_reduce_grad", "bep_set_comm_sms", "bep_status",
-           "bep_clear_status", "bep_strerror")
+           "bep_weights_destroy", "bep_reduce_grad", "bep_set_comm_sms", "bep_wait_selftest",
+           "bep_status", "bep_clear_status", "bep_strerror")
 
 _lib = None
 _lock = threading.Lock()
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
             "bep_weights_destroy": (None, [vp]),
             "bep_combine_dgates": (ctypes.c_int, [vp, p, p, p, i32, p, vp]),
             "bep_set_comm_sms": (ctypes.c_int, [vp, i32]),
+            "bep_wait_selftest": (ctypes.c_int, [vp, i32, vp]),
             "bep_dispatch_bwd": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_grouped_gemm_dx": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_grouped_gemm_dw": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
@@ -386,6 +387,12 @@ def bep_combine_dgates(ctx: Context, dout, y, dest, dgates, stream=None):
 
 def bep_set_comm_sms(ctx: Context, sms: int):
     _check(load().bep_set_comm_sms(ctx.handle, int(sms)), "bep_set_comm_sms")
+
+
+def bep_wait_selftest(ctx: Context, timeout_us: int, stream=None):
+    """Runs the bounded-wait failure path once: sets BEP_DERR_TIMEOUT after timeout_us."""
+    _check(load().bep_wait_selftest(ctx.handle, int(timeout_us), _stream(stream)),
+           "bep_wait_selftest")
 
 
 def bep_dispatch_bwd(ctx: Context, drecv, dest, dx, stream=None):

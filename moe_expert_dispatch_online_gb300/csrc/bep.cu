@@ -288,6 +288,12 @@ int bep_combine_dgates(bep_ctx* ctx, const uint16_t* dout, const uint16_t* y, co
                                               comm_sms(ctx), as_stream(stream)));
 }
 
+int bep_wait_selftest(bep_ctx* ctx, int32_t timeout_us, void* stream) {
+    if (!ctx || timeout_us < 1 || timeout_us > 10000000) return BEP_ERR_ARG;
+    return cuda_rc(bep::launch_wait_selftest(ctx->ws, (uint64_t)timeout_us * 1000ull,
+                                             as_stream(stream)));
+}
+
 int bep_set_comm_sms(bep_ctx* ctx, int32_t sms) {
     if (!ctx || sms < 0) return BEP_ERR_ARG;
     ctx->comm_sms = sms;

@@ -83,6 +83,7 @@ cudaError_t launch_reduce_grad(const Dims& d, const Workspace& ws, const int32_t
                                float* g_home, float* red, int num_sms, cudaStream_t st);
 // grouped GEMM (gemm.cu)
 cudaError_t gemm_setup(int device);
+cudaError_t launch_wait_selftest(const Workspace& ws, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_t* cu,
                                 const uint16_t* recv, const uint16_t* w_home,
                                 const uint16_t* w_slots, uint16_t* y, int num_sms,

@@ -103,13 +103,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity. false: gave up (timeout
 // here, or another role of this CTA already gave up).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t timeout_ns = kTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             *abort_flag = 1;
             set_status(status, BEP_DERR_TIMEOUT);
             return false;
@@ -272,8 +272,9 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
     __syncthreads();
     int run = s_warp[warp] + incl - sum;
     const int total = s_warp[32];
-    if (total > d.max_tiles) bad = 1;
-    for (int i = lo; i < hi && total <= d.max_tiles; ++i) {
+    // one inconsistent segment anywhere refuses the whole table: nothing is computed
+    const bool ok = !__syncthreads_or(bad) && total <= d.max_tiles;
+    for (int i = lo; i < hi && ok; ++i) {
         int s = 0, l = 0;
         const int n = tiles_of(i, &s, &l);
         const int u = i / d.NROW, rho = i % d.NROW;
@@ -288,8 +289,10 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         }
         run += n;
     }
-    if (bad) set_status(ws.status, BEP_DERR_BOUNDS);
-    if (threadIdx.x == 0) *ws.ntiles = total <= d.max_tiles ? total : 0;
+    if (threadIdx.x == 0) {
+        if (!ok) set_status(ws.status, BEP_DERR_BOUNDS);
+        *ws.ntiles = ok ? total : 0;
+    }
 }
 
 struct GemmParams {
@@ -612,6 +615,21 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     }
 }
 
+// ---------------------------------------------------------------- wait self-test
+// One thread waits, through the GEMM's bounded-wait helper, on an mbarrier that
+// nothing ever arrives on. The wait gives up after timeout_ns, records
+// BEP_DERR_TIMEOUT and the kernel returns: the failure path is exercised without
+// faulting or hanging anything.
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(&bar, 0, &abort_flag, status, timeout_ns);
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -685,6 +703,11 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(const Workspace& ws, uint64_t timeout_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(ws.status, timeout_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t gemm_setup(int device) {
     (void)device;
