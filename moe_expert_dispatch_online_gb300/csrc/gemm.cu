@@ -22,15 +22,15 @@
 //     tile fastest, so neighbouring CTAs share their A tile in L2;
 //   * warp 0 issues TMA loads (128-byte swizzle) into a 4-stage shared-memory
 //     ring guarded by mbarriers;
-//   * warp 1 (one thread) issues tcgen05.mma.kind::f16 (M=128, N=BN<=256, K=16,
+//   * warp 1 (lane 0) issues tcgen05.mma.kind::f16 (M=128, N=BN<=256, K=16,
 //     bf16 in, fp32 accumulate) into one of two TMEM accumulators; tcgen05.commit
 //     frees each stage and publishes each finished tile;
 //   * 4 (DW: 8) epilogue warps drain the other accumulator with tcgen05.ld:
 //     FWD/DX round to bf16 (nearest even) and store only the rows inside the
 //     segment; DW adds the fp32 tile into the gradient rows;
 //   * DW only: a segment's last K block usually extends past the segment, into
-//     the next segment's rows; a fix-up warp zeroes those rows of both operand
-//     tiles in shared memory before the MMA may read them.
+//     the next segment's rows; the 32 lanes of warp 1 zero those rows of both
+//     operand tiles in shared memory before lane 0 issues the MMAs that read them.
 // Every mbarrier wait is bounded (2 s on the global timer); on expiry the CTA
 // records BEP_DERR_TIMEOUT, every role leaves its loop, and TMEM is freed.
 
@@ -54,11 +54,10 @@ template <int MODE>
 struct ModeCfg {
     static constexpr bool kAmn = MODE == kDw;          // A operand MN-major (recv^T)
     static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
-    static constexpr bool kFix = MODE == kDw;          // tail-zeroing warp
     static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
     static constexpr int kStages = 4;
     static constexpr int kOutBufs = MODE == kDw ? 1 : 0;   // fp32 staging boxes per epilogue warp
-    static constexpr int kWarps = 2 + kEpiWarps + (kFix ? 1 : 0);
+    static constexpr int kWarps = 2 + kEpiWarps;
     static constexpr int kThreads = 32 * kWarps;
 };
 
@@ -363,10 +362,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     uint64_t* bars = reinterpret_cast<uint64_t*>(smO + CF::kEpiWarps * CF::kOutBufs * kOutBox);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
-    uint64_t* fix = bars + 2 * kStages;
-    uint64_t* tfull = bars + 3 * kStages;
-    uint64_t* tempty = bars + 3 * kStages + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 4);
+    uint64_t* tfull = bars + 2 * kStages;
+    uint64_t* tempty = bars + 2 * kStages + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int32_t* status = p.status;
 
@@ -375,7 +373,6 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&fix[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -405,13 +402,28 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+            // The boxes of K block kb of unit u: op(map, piece, c0, c1), pieces 0-1
+            // are the A tile's 8 KB chunks, pieces 2.. the B tile's.
+            auto kblock = [&](const Unit& u, int kb, auto&& op) {
+                const int n0 = u.nt * BN;
+                const CUtensorMap* tmB = (MODE == kDw || p.vm || u.t.wsel >= 0) ? &tmB0 : &tmB1;
+                const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
+                if (MODE == kFwd) {
+                    op(&tmA, 0, kb * kBK, u.t.row0);
+                    for (int c = 0; c < BN / 64; ++c) op(tmB, 2 + c, n0 + c * 64, brow0 + kb * kBK);
+                } else if (MODE == kDx) {
+                    op(&tmA, 0, kb * kBK, u.t.row0);
+                    op(tmB, 2, kb * kBK, brow0 + n0);
+                } else {
+                    const int r0 = u.t.row0 + kb * kBK;
+                    for (int c = 0; c < 2; ++c) op(&tmA, c, u.mblk * kBM + c * 64, r0);
+                    for (int c = 0; c < BN / 64; ++c) op(&tmB0, 2 + c, n0 + c * 64, r0);
+                }
+            };
             uint32_t s = 0, ph = 0;
             bool live = true;
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
-                const int n0 = u.nt * BN;
-                const CUtensorMap* tmB = (MODE == kDw || p.vm || u.t.wsel >= 0) ? &tmB0 : &tmB1;
-                const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
@@ -420,22 +432,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
                     uint8_t* a_dst = smA + s * kABytes;
                     uint8_t* b_dst = smB + s * b_bytes;
-                    if (MODE == kFwd) {
-                        tma_load_2d(&tmA, &full[s], a_dst, kb * kBK, u.t.row0);
-                        for (int c = 0; c < BN / 64; ++c)
-                            tma_load_2d(tmB, &full[s], b_dst + c * kBChunkBytes, n0 + c * 64,
-                                        brow0 + kb * kBK);
-                    } else if (MODE == kDx) {
-                        tma_load_2d(&tmA, &full[s], a_dst, kb * kBK, u.t.row0);
-                        tma_load_2d(tmB, &full[s], b_dst, kb * kBK, brow0 + n0);
-                    } else {
-                        const int r0 = u.t.row0 + kb * kBK;
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_2d(&tmA, &full[s], a_dst + c * kBChunkBytes,
-                                        u.mblk * kBM + c * 64, r0);
-                        for (int c = 0; c < BN / 64; ++c)
-                            tma_load_2d(&tmB0, &full[s], b_dst + c * kBChunkBytes, n0 + c * 64, r0);
-                    }
+                    kblock(u, kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
+                        uint8_t* dst = piece < 2 ? a_dst + piece * kBChunkBytes
+                                                 : b_dst + (piece - 2) * kBChunkBytes;
+                        tma_load_2d(m, &full[s], dst, c0, c1);
+                    });
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -444,45 +445,65 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
-            uint32_t s = 0, ph = 0;
-            bool live = true;
-            int it = 0;
-            for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
-                const Unit u = unit_at<MODE>(p, unit, NT);
-                const int acc = it & 1;
-                const uint32_t aph = (it >> 1) & 1;
-                if (!mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status)) break;
-                tc_fence_after();
-                const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
-                for (int kb = 0; kb < u.kb_n; ++kb) {
-                    if (!mbar_wait(&full[s], ph, s_abort, status)) {
-                        live = false;
-                        break;
+        // ---------------------------------------------------- MMA issuer (lane 0)
+        // DW: the last K block of a segment usually holds rows of the next
+        // segment past `tail`. Only its first ceil(tail/16) K steps are issued;
+        // the rows of the last issued step past `tail` (at most 15) are zeroed in
+        // both operand tiles by all 32 lanes (whole 128-byte rows, so the
+        // swizzle does not matter) before lane 0 issues the MMAs.
+        const uint32_t idesc = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
+        uint32_t s = 0, ph = 0;
+        bool live = true;
+        int it = 0;
+        for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
+            const Unit u = unit_at<MODE>(p, unit, NT);
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
+            tc_fence_after();
+            const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
+            for (int kb = 0; kb < u.kb_n; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, s_abort, status))) {
+                    live = false;
+                    break;
+                }
+                const bool last = MODE == kDw && kb == u.kb_n - 1;
+                const int ksteps = last ? (u.tail + 15) / 16 : kBK / 16;
+                if (last && (u.tail & 15)) {
+                    const int nrow = 16 - (u.tail & 15);
+                    const int nchunk = 2 + BN / 64;            // A: 2 chunks, B: BN/64 chunks
+                    const int n16 = nrow * 8 * nchunk;         // 16-byte pieces to clear
+                    for (int i = lane; i < n16; i += 32) {
+                        const int piece = i & 7;
+                        const int rc = i >> 3;
+                        const int r = u.tail + rc % nrow;
+                        const int c = rc / nrow;
+                        uint8_t* base = c < 2 ? smA + s * kABytes + c * kBChunkBytes
+                                              : smB + s * b_bytes + (c - 2) * kBChunkBytes;
+                        *reinterpret_cast<uint4*>(base + r * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    // DW: the fix-up warp releases every stage (after zeroing a tail),
-                    // once per use, so fix[s] runs in the same phase as full[s].
-                    if (CF::kFix && !mbar_wait(&fix[s], ph, s_abort, status)) {
-                        live = false;
-                        break;
-                    }
+                    // generic-proxy stores become visible to the tensor core's async proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
+                if (lane == 0) {
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smA + s * kABytes);
                     const uint32_t b0 = smem_u32(smB + s * b_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
-                                 idesc, (kb | kk) != 0);
+                        if (kk < ksteps)
+                            mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
+                                     idesc, (kb | kk) != 0);
                     mma_commit(&empty[s]);
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
                 }
-                if (live) mma_commit(&tfull[acc]);
+                __syncwarp();
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
+            if (live && lane == 0) mma_commit(&tfull[acc]);
         }
     } else if (warp < 2 + CF::kEpiWarps) {
         // ---------------------------------------------------- epilogue
@@ -557,49 +578,6 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         // DW: every reduce this warp issued has been applied before the CTA ends
         if (MODE == kDw && lane == 0) bulk_wait_all();
         __syncwarp();
-    } else if (CF::kFix) {
-        // ---------------------------------------------------- tail fix-up (DW)
-        // The last K block of a segment holds rows of the next segment past
-        // `tail`; zero them in both operand tiles (whole 128-byte rows, so the
-        // swizzle does not matter) before the MMA reads the stage. The warp
-        // takes part in every stage (waits full[s], releases fix[s]) so it can
-        // never drift a whole phase away from the ring: a parity wait only
-        // tells apart two consecutive phases.
-        uint32_t s = 0, ph = 0;
-        bool live = true;
-        for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
-            const Unit u = unit_at<MODE>(p, unit, NT);
-            for (int kb = 0; kb < u.kb_n; ++kb) {
-                const bool got = mbar_wait(&full[s], ph, s_abort, status);
-                __syncwarp();
-                if (!__all_sync(0xffffffffu, got)) {
-                    live = false;
-                    break;
-                }
-                if (kb == u.kb_n - 1 && u.tail < kBK) {
-                    const int nrow = kBK - u.tail;
-                    const int nchunk = 2 + BN / 64;            // A: 2 chunks, B: BN/64 chunks
-                    const int n16 = nrow * 8 * nchunk;         // 16-byte pieces to clear
-                    for (int i = lane; i < n16; i += 32) {
-                        const int piece = i & 7;
-                        const int rc = i >> 3;
-                        const int r = u.tail + rc % nrow;
-                        const int c = rc / nrow;
-                        uint8_t* base = c < 2 ? smA + s * kABytes + c * kBChunkBytes
-                                              : smB + s * b_bytes + (c - 2) * kBChunkBytes;
-                        *reinterpret_cast<uint4*>(base + r * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    // generic-proxy stores become visible to the tensor core's async proxy
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&fix[s]);
-                if (++s == kStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
     }
 
     __syncthreads();
@@ -684,7 +662,7 @@ size_t smem_bytes(int BN) {
     using CF = ModeCfg<MODE>;
     const size_t stage_out = (size_t)CF::kEpiWarps * CF::kOutBufs * kOutBox;
     return 1024 + (size_t)CF::kStages * (kABytes + BN * kBK * 2) + stage_out +
-           (3 * CF::kStages + 4) * 8 + 16;
+           (2 * CF::kStages + 4) * 8 + 16;
 }
 
 int tmem_cols_for(int BN) {
