@@ -110,6 +110,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def flat_dev(xs):
+    """max_i |x_i - mean| / mean, or None for no values."""
+    if not xs:
+        return None
+    m = statistics.mean(xs)
+    return max(abs(x - m) for x in xs) / m
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
@@ -430,6 +438,11 @@ def run_gpu(args, rank, world, local_rank):
         "sweep": per_target,
         "flatness_max_over_min": (max(v["step_ms"] for v in per_target.values()) /
                                   min(v["step_ms"] for v in per_target.values())) if per_target else None,
+        # largest deviation of one maxvio target's step time from the mean over the targets
+        # (the +-10% flatness criterion), for the whole step and for dispatch+combine alone
+        "flatness_dev_from_mean": flat_dev([v["step_ms"] for v in per_target.values()]),
+        "dispatch_combine_dev_from_mean": flat_dev(
+            [v["dispatch_ms"] + v["combine_ms"] for v in per_target.values()]),
         "roofline": {"kernel": "grouped_gemm", "bound": "tensor", "achieved": gemm_tflops,
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_sus"],
                      "peak_source": f"{pk['src']} bf16 sustained (kernel timed inside a long step)",
