@@ -45,7 +45,8 @@ namespace {
 
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBChunkBytes = 64 * kBK * 2;      // 8 KB: 64 rows x 64 columns of bf16
-constexpr int kOutBox = 32 * 32 * 4;            // DW epilogue: 32 rows x 32 fp32 columns
+constexpr int kOutBox = 32 * 128;               // epilogue staging box: 32 rows x 128 B
+                                                // (DW: 32 fp32 columns; FWD/DX: 64 bf16 columns)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2 };
@@ -56,7 +57,7 @@ struct ModeCfg {
     static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
     static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
     static constexpr int kStages = 4;
-    static constexpr int kOutBufs = MODE == kDw ? 1 : 0;   // fp32 staging boxes per epilogue warp
+    static constexpr int kOutBufs = 1;                     // staging boxes per epilogue warp
     static constexpr int kWarps = 2 + kEpiWarps;
     static constexpr int kThreads = 32 * kWarps;
 };
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     uint8_t* smA = smem;
     constexpr int kStages = CF::kStages;
     uint8_t* smB = smem + kStages * kABytes;
-    uint8_t* smO = smB + kStages * b_bytes;   // DW: a 32x32 fp32 staging box per epilogue warp
+    uint8_t* smO = smB + kStages * b_bytes;   // a 4 KB staging box per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smO + CF::kEpiWarps * CF::kOutBufs * kOutBox);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
@@ -521,16 +522,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             const Unit u = unit_at<MODE>(p, unit, NT);
-            const int row = q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_stride);
             if (MODE == kDw) {
                 // 32 rows x 32 columns at a time: stage the fp32 box in shared memory
                 // (128-byte swizzle: 16-byte piece j of row r sits at j ^ (r & 7)), then
                 // one lane has the memory system add it to the gradient rows (one fp32
                 // rounding per element). Measured alternatives -- two staging boxes per
-                // warp with a 3-stage operand ring, per-thread red.global.add.v4, and a
-                // load/add/store on the LSU path with the next chunk in flight -- were
-                // slower on the S=8192, E=384 workload.
+                // warp with a 3-stage operand ring, red.global.add.v4 per row or read back
+                // coalesced, and a load/add/store on the LSU path with the next chunk in
+                // flight -- were slower or no faster on the S=8192, E=384 workload.
                 const CUtensorMap* tmO = u.t.wsel >= 0 ? &tmO0 : &tmO1;
                 const int orow0 = (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel)) * p.H +
                                   u.mblk * kBM + q * 32;
@@ -552,13 +552,21 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     }
                 }
             } else {
-                const bool valid = row < u.t.rows;
-                uint16_t* yrow = p.out + (int64_t)(u.t.row0 + row) * p.N + (int64_t)u.nt * BN;
-                for (int c0 = c_lo; c0 < c_lo + cspan; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + c0);
+                // 64 columns at a time: round to bf16 (nearest even) and stage the warp's
+                // 32 rows x 128 B in shared memory (16-byte piece j of row r sits at
+                // j ^ (r & 7)); read them back a row per 8 lanes so that each store
+                // instruction writes four whole 128-byte lines. Rows past the segment end
+                // belong to the next segment's tile and are skipped.
+                const int nvalid = u.t.rows - q * 32;   // this warp's rows inside the segment
+                uint8_t* stg = smO + e * kOutBox;
+                uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
+                const int rsub = lane >> 3, piece = lane & 7;
+                uint16_t* ybase = p.out + ((int64_t)u.t.row0 + q * 32) * p.N + (int64_t)u.nt * BN;
+                for (int c0 = c_lo; c0 < c_lo + cspan && nvalid > 0; c0 += 64) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)(c0 + 32 * h), r);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 o;
@@ -566,9 +574,18 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                             o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
                             o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
                             o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                            dst[v] = o;
+                            srow[(4 * h + v) ^ (lane & 7)] = o;
                         }
                     }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = 4 * k + rsub;
+                        const uint4 o = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
+                        if (rr < nvalid)
+                            *reinterpret_cast<uint4*>(ybase + (int64_t)rr * p.N + c0 + piece * 8) = o;
+                    }
+                    __syncwarp();   // the box is read back before the next chunk overwrites it
                 }
             }
             tc_fence_before();
