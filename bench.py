@@ -36,7 +36,11 @@ METRIC = "dispatch+combine tokens/s and HBM GB/s vs peak, maxvio 0.2-20, 1 GB300
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the forward
 # grouped GEMM, from one ncu capture of this bench at full size (mean over the four
 # routings). Must be reset to None whenever that kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 24.85e9}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 25.12e9}
+
+# Input sets the end-to-end loop keeps on the device: uploads run up to this many steps
+# ahead of compute (1.2 GB per set at the S=8192, E=384 workload).
+E2E_DEPTH = 6
 
 
 def peaks():
@@ -321,37 +325,44 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers. Every step uploads its
     # inputs (topk, x, gates, dOut) from pinned host memory and downloads its output.
-    # Inputs and outputs are double-buffered on the device and the copies run on a
-    # second stream, so step i+2's upload and step i's download overlap compute.
+    # The uploads run on their own stream up to E2E_DEPTH steps ahead of compute, into
+    # E2E_DEPTH device input sets; the downloads run on a third stream. Host-to-device
+    # copies on this platform now and then stall for tens of milliseconds (one copy in
+    # 20-40 took 60-70 ms instead of 5.7 ms); the look-ahead absorbs such a stall the way
+    # an input pipeline does, and every step's inputs are still copied inside the timed
+    # region.
     x_h = x.cpu().pin_memory()
     dout_h = dout.cpu().pin_memory()
     gates_h = gates.cpu().pin_memory()
     topks_h = [t.cpu().pin_memory() for t in topks]
     out_h = [torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory() for _ in range(2)]
-    dbl = [dict(topk=torch.empty_like(topks[0]), x=torch.empty_like(x), g=torch.empty_like(gates),
-                dout=torch.empty_like(dout), out=torch.empty_like(buf.out)) for _ in range(2)]
+    depth = E2E_DEPTH
+    sets = [dict(topk=torch.empty_like(topks[0]), x=torch.empty_like(x), g=torch.empty_like(gates),
+                 dout=torch.empty_like(dout), out=torch.empty_like(buf.out)) for _ in range(depth)]
     h2d = x_h.numel() * 2 + dout_h.numel() * 2 + gates_h.numel() * 4 + topks_h[0].numel() * 4
     d2h = out_h[0].numel() * 2
-    copy_stream = torch.cuda.Stream(device=dev)
-    loaded = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
+    loaded = [torch.cuda.Event() for _ in range(depth)]
+    released = [torch.cuda.Event() for _ in range(depth)]
 
     def upload(i):
-        b = dbl[i % 2]
-        with torch.cuda.stream(copy_stream):
+        b = sets[i % depth]
+        with torch.cuda.stream(up_stream):
+            if i >= depth:   # step i - depth has consumed this set and its output is read back
+                up_stream.wait_event(released[i % depth])
             b["topk"].copy_(topks_h[i % len(topks_h)], non_blocking=True)
             b["x"].copy_(x_h, non_blocking=True)
             b["g"].copy_(gates_h, non_blocking=True)
             b["dout"].copy_(dout_h, non_blocking=True)
-            loaded[i % 2].record(copy_stream)
+            loaded[i % depth].record(up_stream)
 
     def e2e_run(n):
-        upload(0)
-        if n > 1:
-            upload(1)
+        for i in range(min(n, depth)):
+            upload(i)
         for i in range(n):
-            b = dbl[i % 2]
-            stream.wait_event(loaded[i % 2])
+            b = sets[i % depth]
+            stream.wait_event(loaded[i % depth])
             bep.bep_plan(ctx, b["topk"], buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio,
                          stream)
             bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
@@ -360,13 +371,14 @@ def run_gpu(args, rank, world, local_rank):
             bep.bep_combine(ctx, buf.y, buf.dest, b["g"], b["out"], stream)
             bep.bep_combine_bwd(ctx, b["dout"], buf.dest, b["g"], buf.dy, stream)
             bep.bep_reduce_grad(ctx, buf.slot_expert, g_home, red, stream)
-            consumed[i % 2].record(stream)
-            copy_stream.wait_event(consumed[i % 2])
-            with torch.cuda.stream(copy_stream):
+            down_stream.wait_stream(stream)
+            with torch.cuda.stream(down_stream):
                 out_h[i % 2].copy_(b["out"], non_blocking=True)
-            if i + 2 < n:
-                upload(i + 2)
-        stream.wait_stream(copy_stream)
+                released[i % depth].record(down_stream)
+            if i + depth < n:
+                upload(i + depth)
+        stream.wait_stream(up_stream)
+        stream.wait_stream(down_stream)
 
     e2e_run(min(args.warmup, 3))
     torch.cuda.synchronize()
@@ -374,7 +386,8 @@ def run_gpu(args, rank, world, local_rank):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    copy_stream.wait_event(e0)
+    up_stream.wait_event(e0)
+    down_stream.wait_event(e0)
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
