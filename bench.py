@@ -122,6 +122,56 @@ def flat_dev(xs):
     return max(abs(x - m) for x in xs) / m
 
 
+def run_inference(bep, synth, w_home, stream, dev, reps):
+    """Plan, prefetch, dispatch, grouped GEMM and combine at the inference workload (S=512,
+    B=4, hot experts on one home group), timing the GEMM per maxvio target. Algorithmic GEMM
+    bytes: receive rows read once, Y written once, and one weight row per non-empty segment."""
+    import torch
+    name = "infer_r8_e384_b4"
+    wl = synth.WORKLOADS[name]
+    R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+    cfg = bep.Config(R, E, B, K, S, H, Hp, wl.mode)
+    ctx = bep.Context(cfg)
+    buf = bep.Buffers(cfg, dev)
+    x = synth.tokens_device((R, S, H), 11, device=dev)
+    gates = torch.from_numpy(synth.gates_host(R, S, K, 11)).to(dev)
+    w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=dev)
+    res = {"workload": f"{name} (R={R}, S={S}/rank, E={E}, K={K}, H={H}, H'={Hp}, B={B}, inference)"}
+    for target in synth.MAXVIO_TARGETS[name]:
+        topk = torch.from_numpy(synth.routing(wl, target, 0)).to(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for i in range(reps + 1):
+            bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
+            bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+            bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+            if i > 0:
+                ev[i - 1][0].record(stream)
+            bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
+            if i > 0:
+                ev[i - 1][1].record(stream)
+            bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+        torch.cuda.synchronize()
+        st = bep.bep_status(ctx, stream)
+        if st:
+            raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+        cu = buf.cu_seqlens
+        nseg = int((cu[:, 1:] > cu[:, :-1]).sum().item())
+        # overflow segments: non-empty rows of [0, E) outside the rank's own home group
+        nonempty = (cu[:, 1:E + 1] > cu[:, :E]).cpu()
+        home = (torch.arange(E) // (E // R))[None, :] == torch.arange(R)[:, None]
+        overflow = int((nonempty & ~home).sum().item())
+        ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        byts = nseg * H * Hp * 2 + R * S * K * (H + Hp) * 2
+        res[str(target)] = {"maxvio": round(float(buf.maxvio.item()), 4), "segments": nseg,
+                            "gemm_ms": ms, "gemm_gbs": byts / (ms * 1e-3) / 1e9,
+                            "frac_hbm": byts / (ms * 1e-3) / 1e9 / peaks()["hbm"],
+                            "tflops": 2.0 * R * S * K * H * Hp / (ms * 1e-3) / 1e12,
+                            "overflow_segments": overflow}
+    del ctx, buf, x, w_slots
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
@@ -287,6 +337,35 @@ def run_gpu(args, rank, world, local_rank):
         comm32 = {"sms": 32, "dispatch_ms": d32, "combine_ms": c32,
                   "tokens_per_s": R * S / ((d32 + c32) * 1e-3),
                   "dispatch_gbs": db / (d32 * 1e-3) / 1e9, "combine_gbs": cb / (c32 * 1e-3) / 1e9}
+
+    # ---- the weighted combine on H-wide rows (the down projection's output, the EP payload)
+    comb_h = None
+    if not args.no_backward:
+        out_h_dev = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+        nb = min(args.steps, 2 * len(topks))
+        hev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
+        for i in range(nb + 1):
+            bep.bep_plan(ctx, topks[i % len(topks)], buf.cu_seqlens, buf.slot_expert, buf.dest,
+                         buf.maxvio, stream)
+            bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+            if i > 0:
+                hev[i - 1][0].record(stream)
+            bep.bep_combine(ctx, buf.recv, buf.dest, gates, out_h_dev, stream)
+            if i > 0:
+                hev[i - 1][1].record(stream)
+        torch.cuda.synchronize()
+        ch_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in hev)
+        chb = R * S * K * H * 2 + R * S * H * 2 + R * S * K * 8
+        comb_h = {"D": H, "ms": ch_ms, "gbs": chb / (ch_ms * 1e-3) / 1e9,
+                  "frac_hbm": chb / (ch_ms * 1e-3) / 1e9 / peaks()["hbm"]}
+        del out_h_dev
+        torch.cuda.empty_cache()
+
+    # ---- inference mode with overflow (B = 4 < E/R, S = 512): the grouped GEMM reads each
+    # active weight row once and is bound by HBM, not by the tensor cores
+    infer = None
+    if not args.no_backward and args.workload == WORKLOAD:
+        infer = run_inference(bep, synth, w_home, stream, dev, min(args.steps, 8))
 
     # ---- the VM group GEMM through the weight store's aliased [E+B, H, H'] views
     vmg = None
@@ -467,6 +546,8 @@ def run_gpu(args, rank, world, local_rank):
         "backward": bwd,
         "comm_sms_32": comm32,
         "vm_group_gemm": vmg,
+        "combine_d_h": comb_h,
+        "inference": infer,
     }
     return result
 
