@@ -1,0 +1,148 @@
+"""The three grouped GEMMs on hand-made cu_seqlens tables whose segment lengths
+cover every residue of a segment end against the kernels' blocking: the 16-row
+K step and 64-row K block of the weight-gradient GEMM (its last block issues
+only the steps it holds and zeroes the rest of the last step), and the 128-row
+M tile of the forward and input-gradient GEMMs (rows past a segment end belong
+to the next segment and must not be written). Compared per segment / weight
+row with the binary64 oracle; rows outside every segment keep their contents."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+RTOL = 2e-2
+
+# R=2, E=8, B=4 (training), K=2, S=1024: C=2048 slots per rank; H=256, H'=128
+R, E, B, K, S, H, HP = 2, 8, 4, 2, 1024, 256, 128
+C = S * K
+LENGTHS = [
+    [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12],                  # rank 0: 78 rows
+    [13, 14, 15, 16, 63, 64, 65, 127, 128, 129, 257, 0],      # rank 1: 891 rows
+]
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(DEV).view(
+        torch.bfloat16)
+
+
+def host_u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def table():
+    cu = np.zeros((R, E + B + 1), np.int32)
+    for u in range(R):
+        cu[u, 1:] = np.cumsum(LENGTHS[u])
+    assert cu[:, -1].max() <= C
+    return cu
+
+
+def context(bep):
+    return bep.Context(bep.Config(R, E, B, K, S, H, HP, 0))
+
+
+def covered(cu):
+    """Boolean mask over the R*C receive rows that lie inside some segment."""
+    m = np.zeros(R * C, bool)
+    for u in range(R):
+        m[u * C:u * C + int(cu[u, -1])] = True
+    return m
+
+
+def test_lengths_cover_every_residue():
+    flat = [n for row in LENGTHS for n in row if n > 0]
+    assert {n % 16 for n in flat} == set(range(16))
+    assert {n % 64 for n in flat} >= {0, 1, 15, 16, 63}
+    assert {n % 128 for n in flat} >= {0, 1, 127}
+
+
+def test_forward_on_ragged_segments(lib):
+    bep = lib
+    ctx = context(bep)
+    cu = table()
+    recv = synth.tokens_host((R * C, H), 301)
+    w_home = synth.weights_host((E, H, HP), 302)
+    w_slots = synth.weights_host((R, B, H, HP), 303)
+    y = torch.full((R * C, HP), -7.0, dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm(ctx, torch.from_numpy(cu).to(DEV), dev_u16(recv), dev_u16(w_home),
+                         dev_u16(w_slots), y)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    ref = oracle.grouped_gemm(recv, w_home, w_slots, cu, E)
+    got = oracle.bf16_to_f32(host_u16(y)).astype(np.float64)
+    for u in range(R):
+        for rho in range(E + B):
+            a, b = u * C + int(cu[u, rho]), u * C + int(cu[u, rho + 1])
+            if a == b:
+                continue
+            err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
+            assert err <= RTOL, (u, rho, b - a, err)
+    assert (got[~covered(cu)] == -7.0).all()
+
+
+def test_input_gradient_on_ragged_segments(lib):
+    bep = lib
+    ctx = context(bep)
+    cu = table()
+    dy = synth.tokens_host((R * C, HP), 311)
+    w_home = synth.weights_host((E, H, HP), 312)
+    w_slots = synth.weights_host((R, B, H, HP), 313)
+    drecv = torch.full((R * C, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, torch.from_numpy(cu).to(DEV), dev_u16(dy), dev_u16(w_home),
+                            dev_u16(w_slots), drecv)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    ref = oracle.grouped_gemm_dx(dy, w_home, w_slots, cu, E)
+    got = oracle.bf16_to_f32(host_u16(drecv)).astype(np.float64)
+    for u in range(R):
+        for rho in range(E + B):
+            a, b = u * C + int(cu[u, rho]), u * C + int(cu[u, rho + 1])
+            if a == b:
+                continue
+            err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
+            assert err <= RTOL, (u, rho, b - a, err)
+    assert (got[~covered(cu)] == 3.0).all()
+
+
+@pytest.mark.parametrize("poison", [False, True])
+def test_weight_gradient_on_ragged_segments(lib, poison):
+    """poison=True fills the receive rows outside every segment with +inf: a tail
+    step that read them unzeroed would turn a gradient row non-finite."""
+    bep = lib
+    ctx = context(bep)
+    cu = table()
+    recv = synth.tokens_host((R * C, H), 321)
+    dy = synth.tokens_host((R * C, HP), 322)
+    if poison:
+        out = ~covered(cu)
+        recv[out] = 0x7F80          # bf16 +inf
+        dy[out] = 0x7F80
+    g0 = synth.normal_host((E, H, HP), 323, 0.5)
+    red0 = synth.normal_host((R, B, H, HP), 324, 0.5)
+    g = torch.from_numpy(g0).to(DEV)
+    red = torch.from_numpy(red0).to(DEV)
+    bep.bep_grouped_gemm_dw(ctx, torch.from_numpy(cu).to(DEV), dev_u16(recv), dev_u16(dy), g, red)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    d_home, d_slots = oracle.grouped_gemm_dw(recv, dy, cu, E, B, H, HP)
+    gh, rh = g.cpu().numpy().astype(np.float64), red.cpu().numpy().astype(np.float64)
+    assert np.isfinite(gh).all() and np.isfinite(rh).all()
+    for e in range(E):
+        if not d_home[e].any():
+            np.testing.assert_array_equal(gh[e], g0[e])
+            continue
+        err = np.linalg.norm(gh[e] - (g0[e] + d_home[e])) / np.linalg.norm(d_home[e])
+        assert err <= RTOL, (e, err)
+    for u in range(R):
+        for j in range(B):
+            if not d_slots[u, j].any():
+                np.testing.assert_array_equal(rh[u, j], red0[u, j])
+                continue
+            err = np.linalg.norm(rh[u, j] - (red0[u, j] + d_slots[u, j])) / np.linalg.norm(d_slots[u, j])
+            assert err <= RTOL, (u, j, err)
