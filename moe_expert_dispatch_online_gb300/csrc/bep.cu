@@ -3,7 +3,22 @@
 
 #include <stdlib.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "bep_internal.cuh"
+
+namespace {
+// One NVTX range per call of a compute entry point, named after the call, so the
+// kernels it queues show under that name in nsys / ncu --nvtx. Header-only NVTX:
+// without an attached tool a range costs a pointer check.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
+#define BEP_RANGE(name) const NvtxRange bep_nvtx_range_(name)
 
 struct bep_ctx {
     bep::Dims d;
@@ -151,6 +166,7 @@ void bep_destroy(bep_ctx* ctx) {
 
 int bep_plan(bep_ctx* ctx, const int32_t* topk, int32_t* cu_seqlens, int32_t* slot_expert,
              int32_t* dest, double* maxvio, void* stream) {
+    BEP_RANGE("bep_plan");
     if (!ctx || !cu_seqlens || !maxvio || (ctx->d.R * ctx->d.B > 0 && !slot_expert))
         return BEP_ERR_ARG;
     if (ctx->d.C > 0 && (!topk || !dest)) return BEP_ERR_ARG;
@@ -163,6 +179,7 @@ int bep_plan(bep_ctx* ctx, const int32_t* topk, int32_t* cu_seqlens, int32_t* sl
 
 int bep_prefetch_weight(bep_ctx* ctx, const int32_t* slot_expert, const uint16_t* w_home,
                         uint16_t* w_slots, void* stream) {
+    BEP_RANGE("bep_prefetch_weight");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.R * ctx->d.B == 0) return BEP_OK;
     if (!slot_expert || !w_home || !w_slots) return BEP_ERR_ARG;
@@ -174,6 +191,7 @@ int bep_prefetch_weight(bep_ctx* ctx, const int32_t* slot_expert, const uint16_t
 
 int bep_dispatch(bep_ctx* ctx, const uint16_t* x, const int32_t* dest, uint16_t* recv,
                  void* stream) {
+    BEP_RANGE("bep_dispatch");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!x || !dest || !recv) return BEP_ERR_ARG;
@@ -184,6 +202,7 @@ int bep_dispatch(bep_ctx* ctx, const uint16_t* x, const int32_t* dest, uint16_t*
 
 int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
                      const uint16_t* w_home, const uint16_t* w_slots, uint16_t* y, void* stream) {
+    BEP_RANGE("bep_grouped_gemm");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!cu_seqlens || !recv || !w_home || !y) return BEP_ERR_ARG;
@@ -197,6 +216,7 @@ int bep_grouped_gemm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* re
 
 int bep_grouped_gemm_vm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
                         const uint16_t* w_views, uint16_t* y, void* stream) {
+    BEP_RANGE("bep_grouped_gemm_vm");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!cu_seqlens || !recv || !w_views || !y) return BEP_ERR_ARG;
@@ -208,6 +228,7 @@ int bep_grouped_gemm_vm(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
 
 int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const float* gates,
                 int32_t D, uint16_t* out, void* stream) {
+    BEP_RANGE("bep_combine");
     if (!ctx || D < 8 || D % 8 != 0) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!y || !dest || !gates || !out) return BEP_ERR_ARG;
@@ -219,6 +240,7 @@ int bep_combine(bep_ctx* ctx, const uint16_t* y, const int32_t* dest, const floa
 
 int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest, const float* gates,
                     int32_t D, uint16_t* dy, void* stream) {
+    BEP_RANGE("bep_combine_bwd");
     if (!ctx || D < 8 || D % 8 != 0) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!dout || !dest || !gates || !dy) return BEP_ERR_ARG;
@@ -230,6 +252,7 @@ int bep_combine_bwd(bep_ctx* ctx, const uint16_t* dout, const int32_t* dest, con
 
 int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, uint16_t* dx,
                      void* stream) {
+    BEP_RANGE("bep_dispatch_bwd");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!drecv || !dest || !dx) return BEP_ERR_ARG;
@@ -241,6 +264,7 @@ int bep_dispatch_bwd(bep_ctx* ctx, const uint16_t* drecv, const int32_t* dest, u
 int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* dy,
                         const uint16_t* w_home, const uint16_t* w_slots, uint16_t* drecv,
                         void* stream) {
+    BEP_RANGE("bep_grouped_gemm_dx");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!cu_seqlens || !dy || !w_home || !drecv) return BEP_ERR_ARG;
@@ -254,6 +278,7 @@ int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
 
 int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
                         const uint16_t* dy, float* g_home, float* red, void* stream) {
+    BEP_RANGE("bep_grouped_gemm_dw");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.mode != BEP_TRAIN) return BEP_ERR_MODE;
     if (ctx->d.H % bep::kBM != 0) return BEP_ERR_SIZE;
@@ -268,6 +293,7 @@ int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
 
 int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, float* red,
                     void* stream) {
+    BEP_RANGE("bep_reduce_grad");
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.R * ctx->d.B == 0) return BEP_OK;
     if (!slot_expert || !g_home || !red) return BEP_ERR_ARG;
@@ -279,6 +305,7 @@ int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, flo
 
 int bep_combine_dgates(bep_ctx* ctx, const uint16_t* dout, const uint16_t* y, const int32_t* dest,
                        int32_t D, float* dgates, void* stream) {
+    BEP_RANGE("bep_combine_dgates");
     if (!ctx || D < 8 || D % 8 != 0) return BEP_ERR_ARG;
     if (ctx->d.C == 0) return BEP_OK;
     if (!dout || !y || !dest || !dgates) return BEP_ERR_ARG;
