@@ -39,8 +39,8 @@ METRIC = "dispatch+combine tokens/s and HBM GB/s vs peak, maxvio 0.2-20, 1 GB300
 GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 25.12e9}
 
 # Input sets the end-to-end loop keeps on the device: uploads run up to this many steps
-# ahead of compute (1.2 GB per set at the S=8192, E=384 workload).
-E2E_DEPTH = 6
+# ahead of compute (1.5 GB per set at the S=8192, E=384 workload, 18 GB in all).
+E2E_DEPTH = 12
 
 
 def peaks():
@@ -407,7 +407,7 @@ def run_gpu(args, rank, world, local_rank):
     # The uploads run on their own stream up to E2E_DEPTH steps ahead of compute, into
     # E2E_DEPTH device input sets; the downloads run on a third stream. Host-to-device
     # copies on this platform now and then stall for tens of milliseconds (one copy in
-    # 20-40 took 60-70 ms instead of 5.7 ms); the look-ahead absorbs such a stall the way
+    # 20-40 took 60-90 ms instead of 5.7 ms); the look-ahead absorbs such a stall the way
     # an input pipeline does, and every step's inputs are still copied inside the timed
     # region.
     x_h = x.cpu().pin_memory()
@@ -459,7 +459,7 @@ def run_gpu(args, rank, world, local_rank):
         stream.wait_stream(up_stream)
         stream.wait_stream(down_stream)
 
-    e2e_run(min(args.warmup, 3))
+    e2e_run(max(args.warmup, depth))   # every input set used once before the timer starts
     torch.cuda.synchronize()
     dist_barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
