@@ -492,9 +492,15 @@ def run_gpu(args, rank, world, local_rank):
         if not idx:
             continue
         step_ms = [sum(stage_ms[s][i] for s in stages) for i in idx]
+        fwd = ("plan", "prefetch", "dispatch", "gemm", "combine")
+        fwd_ms = [sum(stage_ms[s][i] for s in fwd) for i in idx]
+        fwd_np_ms = [sum(stage_ms[s][i] for s in fwd if s != "prefetch") for i in idx]
         per_target["zipf1.2" if t is None else f"{t:g}"] = {
             "maxvio": round(maxvios[j], 4), "replicas": nrep[j],
             "step_ms": round(statistics.mean(step_ms), 4),
+            # the forward alone (plan ... combine), with and without the prefetch of replicas
+            "forward_ms": round(statistics.mean(fwd_ms), 4),
+            "forward_ms_without_prefetch": round(statistics.mean(fwd_np_ms), 4),
             **{f"{s}_ms": round(statistics.mean(stage_ms[s][i] for i in idx), 4) for s in stages},
         }
     traffic = GEMM_DRAM_BYTES_PER_LAUNCH.get(args.workload)
@@ -535,6 +541,7 @@ def run_gpu(args, rank, world, local_rank):
         "flatness_dev_from_mean": flat_dev([v["step_ms"] for v in per_target.values()]),
         "dispatch_combine_dev_from_mean": flat_dev(
             [v["dispatch_ms"] + v["combine_ms"] for v in per_target.values()]),
+        "forward_dev_from_mean": flat_dev([v["forward_ms"] for v in per_target.values()]),
         "roofline": {"kernel": "grouped_gemm", "bound": "tensor", "achieved": gemm_tflops,
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_sus"],
                      "peak_source": f"{pk['src']} bf16 sustained (kernel timed inside a long step)",
