@@ -117,6 +117,9 @@ def test_plan_bit_exact(lib, name, target, seed):
     (8, 600, 8, 64, 3, 1, "hot"),        # inference, heavy overflow
     (4, 777, 32, 64, 16, 0, "zipf"),     # K = 32 (the limit)
     (64, 40, 2, 128, 2, 0, "zipf"),      # R = 64 (the limit)
+    (64, 512, 32, 2048, 32, 0, "zipf"),   # R, E and K all at their limits
+    (64, 512, 32, 2048, 32, 0, "hot"),    # every token on group 0's first 32 experts
+    (8, 1024, 8, 2048, 4, 1, "hot"),      # inference at E = 2048: overflow from one group
 ])
 def test_plan_edge_cases(lib, R, S, K, E, B, mode, how):
     bep = lib
