@@ -367,6 +367,35 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_backward and args.workload == WORKLOAD:
         infer = run_inference(bep, synth, w_home, stream, dev, min(args.steps, 8))
 
+    # ---- the second projection: the down projection [E+B, H', H] on the same plan (a second
+    # context with H and H' swapped), fed by the first projection's output rows
+    proj2 = None
+    if not args.no_backward:
+        ctx2 = bep.Context(bep.Config(R, E, B, K, S, Hp, H, wl.mode))
+        w_dn = synth.weights_device((E, Hp, H), 13, device=dev)
+        dn_slots = torch.zeros((R, B, Hp, H), dtype=torch.bfloat16, device=dev)
+        y2 = torch.empty((R * S * K, H), dtype=torch.bfloat16, device=dev)
+        nb = min(args.steps, 2 * len(topks))
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
+        for i in range(nb + 1):
+            step(i)            # plan, prefetch, dispatch, up projection, combine, ...
+            bep.bep_prefetch_weight(ctx2, buf.slot_expert, w_dn, dn_slots, stream)
+            if i > 0:
+                pev[i - 1][0].record(stream)
+            bep.bep_grouped_gemm(ctx2, buf.cu_seqlens, buf.y, w_dn, dn_slots, y2, stream)
+            if i > 0:
+                pev[i - 1][1].record(stream)
+        torch.cuda.synchronize()
+        st = bep.bep_status(ctx2, stream)
+        if st:
+            raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+        p2_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in pev)
+        fl = 2.0 * R * S * K * H * Hp
+        proj2 = {"ms": p2_ms, "tflops": fl / (p2_ms * 1e-3) / 1e12,
+                 "frac_bf16_sustained": fl / (p2_ms * 1e-3) / 1e12 / peaks()["bf16_sus"]}
+        del ctx2, w_dn, dn_slots, y2
+        torch.cuda.empty_cache()
+
     # ---- the VM group GEMM through the weight store's aliased [E+B, H, H'] views
     vmg = None
     if not args.no_backward:
@@ -554,6 +583,7 @@ def run_gpu(args, rank, world, local_rank):
         "comm_sms_32": comm32,
         "vm_group_gemm": vmg,
         "combine_d_h": comb_h,
+        "second_projection": proj2,
         "inference": infer,
     }
     return result
