@@ -593,13 +593,18 @@ def run_gpu(args, rank, world, local_rank):
 class CpuSample:
     """The oracle, as it stands, on a bounded sample of the bench workload; each
     stage's cost is scaled to one whole step. Inputs are drawn once; step() times
-    the oracle's work only. Runs single-threaded (BLAS threads pinned to 1)."""
+    the oracle's work only. Runs single-threaded (BLAS threads pinned to 1).
 
-    N_TOK = 256      # tokens in the dispatch / combine sample
-    M_ROWS = 64      # receive rows in the GEMM sample
-    FRAC = 16        # prefetch / reduce_grad run on 1/FRAC of one slot
+    Two sizes: "baseline" (the GPU arm's cpu_baseline, one sample of several seconds
+    of CPU work) and "step" (the reference arm, one smaller sample per timed step)."""
 
-    def __init__(self):
+    SIZES = {  # (tokens for dispatch / combine, GEMM receive rows, prefetch / reduce_grad 1/FRAC slot)
+        "baseline": (16384, 8192, 1),
+        "step": (2048, 256, 4),
+    }
+
+    def __init__(self, size: str = "baseline"):
+        self.N_TOK, self.M_ROWS, self.FRAC = self.SIZES[size]
         import numpy as np
 
         import synth
@@ -669,8 +674,8 @@ class CpuSample:
         }
 
 
-def cpu_samples(steps: int, warmup: int):
-    cs = CpuSample()
+def cpu_samples(steps: int, warmup: int, size: str = "baseline"):
+    cs = CpuSample(size)
     out = []
     for i in range(warmup + steps):
         r = cs.step()
@@ -679,10 +684,10 @@ def cpu_samples(steps: int, warmup: int):
     return out
 
 
-def cpu_baseline_subprocess(steps: int = 1, warmup: int = 0):
+def cpu_baseline_subprocess(steps: int = 1, warmup: int = 0, size: str = "baseline"):
     """The oracle timing in a fresh single-threaded process (BLAS threads 1)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample",
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", size,
                         "--steps", str(steps), "--warmup", str(warmup)], env=env,
                        capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
@@ -694,7 +699,7 @@ def run_reference(args, rank, world):
     """The reference arm: the oracle on the host cores, each step one bounded sample."""
     if rank != 0:
         return None
-    res = cpu_baseline_subprocess(args.steps, args.warmup)
+    res = cpu_baseline_subprocess(args.steps, args.warmup, size="step")
     vals = [r["value"] for r in res if "value" in r]
     v = statistics.mean(vals) if vals else None
     base = res[-1] if res else {}
@@ -748,10 +753,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the separate timing of the backward GEMMs and dispatch backward")
-    ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-sample", choices=tuple(CpuSample.SIZES), default=None,
+                    help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_sample:
-        print(json.dumps(cpu_samples(args.steps, args.warmup)))
+        print(json.dumps(cpu_samples(args.steps, args.warmup, args.cpu_sample)))
         return
     rank, world, local = dist_init()
     if args.impl == "reference":
@@ -762,7 +768,8 @@ def main():
     res = run_gpu(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess()[0].items()
+            # one discarded sample first: it pays the allocator's first-touch costs
+            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess(1, 1)[0].items()
                                    if k in ("value", "unit", "cores", "kind", "sample", "error")}
         print(json.dumps(res))
 
