@@ -242,3 +242,53 @@ def test_forward_and_weight_gradient_exact_at_bench_size_sampled(lib):
         np.testing.assert_array_equal(got, dw[0].astype(np.float32))
     del dy, g, red
     torch.cuda.empty_cache()
+
+
+def test_overflow_rows_exact_at_inference_size_sampled(lib):
+    """S=512, B=4 < E/R, hot experts on group 0 (maxvio 20): segments of remote experts
+    beyond the B slots are overflow rows that read the home weights in place. Forward
+    and input gradient with permutation weights, exact on sampled rows of every rank's
+    overflow, slot and first home segments."""
+    bep = lib
+    torch.cuda.empty_cache()
+    wl, ref, ctx, buf = planned(bep, "infer_r8_e384_b4", 20.0)
+    R, C, E, B, H, Hp, G = wl.R, wl.C, wl.E, wl.B, wl.H, wl.Hp, wl.E // wl.R
+    rng = np.random.default_rng(511)
+    x = synth.tokens_device((R, wl.S, H), 512)
+    dy = synth.tokens_device((R * C, Hp), 513)
+    w_home = perm_weights_device(E, H, Hp)
+    w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots)
+    bep.bep_dispatch(ctx, x, buf.dest, buf.recv)
+    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y)
+    drecv = torch.empty((R * C, H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, dy, w_home, w_slots, drecv)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    inv = np.empty(R * C, np.int64)
+    inv[ref.dest.ravel()] = np.arange(R * wl.S * wl.K) // wl.K
+    sh = shifts(E, H)
+    overflow_seen = 0
+    for u in range(R):
+        segs = [rho for rho in range(E + B) if ref.cu[u, rho + 1] > ref.cu[u, rho]]
+        overflow = [rho for rho in segs if rho < E and rho // G != u]
+        slots = [rho for rho in segs if rho >= E]
+        home = [rho for rho in segs if rho < E and rho // G == u]
+        overflow_seen += len(overflow)
+        for rho in overflow[:6] + slots[:2] + home[:1]:
+            a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+            rows = np.array(sorted(set([a, b - 1] + list(rng.integers(a, b, size=2)))), np.int64)
+            gi = torch.from_numpy(u * C + rows).to(DEV)
+            e = oracle.weight_row_of(rho, u, E, ref.slot_expert)
+            w = host_u16(w_home[e])
+            a_rows = host_u16(x.view(-1, H)[torch.from_numpy(inv[u * C + rows]).to(DEV)])
+            y_ref = oracle.f32_to_bf16(oracle.gemm_rows(a_rows, w).astype(np.float32))
+            np.testing.assert_array_equal(nz(y_ref), nz(a_rows[:, (np.arange(Hp) + sh[e]) % H]))
+            np.testing.assert_array_equal(nz(host_u16(buf.y[gi])), nz(y_ref))
+            dy_rows = host_u16(dy[gi])
+            d_ref = oracle.f32_to_bf16(oracle.gemm_rows(dy_rows, np.ascontiguousarray(w.T))
+                                       .astype(np.float32))
+            np.testing.assert_array_equal(nz(host_u16(drecv[gi])), nz(d_ref))
+    assert overflow_seen > 0      # the routing does produce overflow rows
+    del x, dy, w_home, w_slots, drecv
+    torch.cuda.empty_cache()
