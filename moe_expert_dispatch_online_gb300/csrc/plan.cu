@@ -14,9 +14,11 @@
 //   descending, ties by lower g. Pop a recipient, attach it to the current
 //   donor; a donor that overshoots re-enters at the front of the deque with
 //   its new deficit and the next donor takes over.
-//   Group g's slots are listed expert-major, then by (rank, token): g keeps
-//   the first C - inflow_g, each child takes the next `flow` in assignment
-//   order. A replica of expert e on child u sits in slot e - parent(u)*G
+//   Group g's slots are listed expert by expert, the experts in ascending
+//   token count (ties: lower id), each expert's slots in (rank, token) order:
+//   g keeps the first C - inflow_g, each child takes the next `flow` in
+//   assignment order. The moving tail holds the group's largest experts, so a
+//   child's range touches few experts and few replicas are planned. A replica of expert e on child u sits in slot e - parent(u)*G
 //   (training) or, for inference, in one of B slots given to u's B most-loaded
 //   remote experts (ties: lower id; slots in ascending id) with the rest
 //   overflowing onto home row e.
@@ -194,13 +196,21 @@ __global__ void __launch_bounds__(kSolveThreads) plan_solve_kernel(Dims d, Works
         *maxvio = rsk ? (double)((int64_t)E * sMax - rsk) / (double)rsk : 0.0;
     }
 
-    // 2. group loads and each expert's start inside its group's list
+    // 2. group loads, and each expert's start inside its group's list: the tokens
+    //    of the group's experts with a smaller count, or an equal count and a lower id
+    for (int e = tid; e < E; e += nth) {
+        const int g0 = (e / G) * G;
+        const int te = sT[e];
+        int64_t start = 0;
+        for (int f = g0; f < g0 + G; ++f) {
+            const int tf = sT[f];
+            if (tf < te || (tf == te && f < e)) start += tf;
+        }
+        sGS[e] = (int32_t)start;
+    }
     if (tid < R) {
         int64_t run = 0;
-        for (int e = tid * G; e < (tid + 1) * G; ++e) {
-            sGS[e] = (int32_t)run;
-            run += sT[e];
-        }
+        for (int e = tid * G; e < (tid + 1) * G; ++e) run += sT[e];
         sL[tid] = run;
     }
     __syncthreads();

@@ -214,9 +214,13 @@ int oracle_tree(int R, const int64_t* L, int64_t C, int32_t* parent, int64_t* in
 // Step order:
 //  1. histogram, group loads L_g;
 //  2. the tree (plan_tree);
-//  3. group g's slots listed expert-major, then by (r, t): home g keeps the
-//     first C - inflow[g], each child takes the next `flow` entries in the
-//     order the children were assigned;
+//  3. group g's slots listed expert by expert, the group's experts in
+//     ascending token count (ties: lower id), each expert's slots in (r, t)
+//     order: home g keeps the first C - inflow[g], each child takes the next
+//     `flow` entries in the order the children were assigned. The tail that
+//     moves therefore holds the group's largest experts, so each child's range
+//     touches few experts and few replicas are needed ("a small number of
+//     redundant experts", [P4] "The core idea");
 //  4. rows: a home slot of expert e uses row e. A replica on child u:
 //     TRAIN: slot j = e - parent[u]*G, row E + j.
 //     INFER: u's remote experts ranked by slot count descending, ties by
@@ -271,9 +275,13 @@ int oracle_plan(int R, int E, int B, int K, int S, int mode, const int32_t* topk
                 bounds.push_back({pos, ed.child});
             }
         if (pos != L[g]) return OR_ERR_INFEASIBLE;
+        std::vector<int> ex;
+        for (int e = g * G; e < (g + 1) * G; ++e) ex.push_back(e);
+        std::stable_sort(ex.begin(), ex.end(),
+                         [&](int a, int b2) { return T[a] < T[b2]; });  // stable: ties keep lower id first
         int64_t q = 0;
         size_t b = 0;
-        for (int e = g * G; e < (g + 1) * G; ++e)
+        for (int e : ex)
             for (int64_t i : by_expert[e]) {
                 while (q >= bounds[b].first) ++b;
                 owner[i] = bounds[b].second;

