@@ -31,6 +31,9 @@
 //   * DW only: a segment's last K block usually extends past the segment, into
 //     the next segment's rows; the 32 lanes of warp 1 zero those rows of both
 //     operand tiles in shared memory before lane 0 issues the MMAs that read them.
+// When 256 divides H and H', DW runs instead on clusters of two CTAs that share
+// each 256 x 256 gradient tile (grouped_gemm_dw_pair_kernel, cta_group::2): half
+// the operand bytes per SM and a six-stage ring.
 // Every mbarrier wait is bounded (2 s on the global timer); on expiry the CTA
 // records BEP_DERR_TIMEOUT, every role leaves its loop, and TMEM is freed.
 
@@ -197,6 +200,77 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// ---- SM pairs (a cluster of two CTAs running one cta_group::2 MMA stream)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_rank(uint64_t* bar, uint32_t rank) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr(bar, rank))
+                 : "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar_cl: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cl, void* dst, int c0,
+                                                 int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_zero16(uint32_t addr_cl) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr_cl), "r"(0) : "memory");
+}
+
+// One MMA of the pair: M = 256 rows, 128 from each CTA's A tile; N columns, N/2 from each
+// CTA's B tile; each CTA's TMEM receives its own 128 rows. Issued by one thread of CTA 0.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in both CTAs of the pair when every MMA
+// issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
         : "memory");
 }
 
@@ -610,6 +684,253 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     }
 }
 
+// ---------------------------------------------------------------- DW on SM pairs
+// The weight gradient with each 256 x 256 output tile shared by a cluster of two
+// CTAs on neighbouring SMs (tcgen05 cta_group::2). CTA r of the pair loads, per
+// 64-row K block, its 128 columns h of recv (A) and its 128 columns h' of dY (B):
+// 32 KB per stage instead of the 48 KB one CTA needs for a 128 x 256 tile, so a
+// six-stage ring fits where the single-CTA kernel holds four. One thread of CTA 0
+// issues M=256, N=256 MMAs that read both CTAs' tiles; each CTA's TMEM receives
+// its own 128 gradient rows, and each CTA's 8 epilogue warps add them into the
+// gradient exactly as the single-CTA kernel does (same tiles of 32 x 32 fp32, same
+// K order, so the sums are the same bit for bit).
+//   barriers        owner   arrivals
+//   full[s]         CTA 0   CTA 0's producer (expect_tx of both CTAs' bytes) + both CTAs' TMA bytes
+//   empty[s]        both    the MMA thread's multicast commit
+//   tfull[a]        both    the MMA thread's multicast commit at the end of a unit
+//   tempty[a]       CTA 0   the 8 epilogue warps of each CTA
+// CTA 1's loads count on CTA 0's full barrier, so CTA 0 knows when the whole stage
+// is in; CTA 0's MMA warp then zeroes a segment's tail rows in both CTAs' tiles
+// (CTA 1's through distributed shared memory). Every wait is bounded; the CTAs
+// meet at a cluster barrier before TMEM is freed and either exits.
+constexpr int kPairStages = 6;
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
+constexpr int kPairHalf = 2 * kBChunkBytes;   // 16 KB: one CTA's A (or B) tile of a K block
+constexpr int kPairBN = 256;
+constexpr int kPairBM = 256;
+
+__global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmR,
+    const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* smA = smem;
+    uint8_t* smB = smA + kPairStages * kPairHalf;
+    uint8_t* smO = smB + kPairStages * kPairHalf;   // a 4 KB staging box per epilogue warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smO + kPairEpiWarps * kOutBox);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + 2 * kPairStages;
+    uint64_t* tfull = bars + 3 * kPairStages;
+    uint64_t* tempty = bars + 3 * kPairStages + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * kPairStages + 4);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int32_t* status = p.status;
+    const uint32_t rank = cluster_rank();
+    const bool lead = rank == 0;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 2 * kPairEpiWarps);
+        }
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        // one warp of each CTA performs the pair's allocation together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(s_tmem)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before any remote arrive or multicast commit
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    const int NT = p.N / kPairBN;
+    const int per_seg = (p.H / kPairBM) * NT;
+    const int total = *p.ntiles * per_seg;
+    const int cl0 = (int)cluster_id(), ncl = (int)cluster_count();
+    const int acc_stride = p.tmem_cols / 2;
+    auto unit_of = [&](int unit, MTile* t, int* mp, int* nt, int* kb_n, int* tail) {
+        const int seg = unit / per_seg;
+        const int rem = unit - seg * per_seg;
+        *t = p.tiles[seg];
+        *mp = rem / NT;
+        *nt = rem - *mp * NT;
+        *kb_n = (t->rows + kBK - 1) / kBK;
+        *tail = t->rows - (*kb_n - 1) * kBK;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (each CTA its own half)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+            uint32_t s = 0, ph = 0;
+            bool live = true;
+            for (int unit = cl0; unit < total && live; unit += ncl) {
+                MTile t;
+                int mp, nt, kb_n, tail;
+                unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
+                const int h0 = mp * kPairBM + (int)rank * 128;
+                const int n0 = nt * kPairBN + (int)rank * 128;
+                for (int kb = 0; kb < kb_n; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
+                        live = false;
+                        break;
+                    }
+                    // CTA 0's barrier counts both CTAs' 32 KB
+                    if (lead) mbar_arrive_expect_tx(&full[s], 4 * kPairHalf);
+                    const uint32_t bar = cluster_addr(&full[s], 0);
+                    const int r0 = t.row0 + kb * kBK;
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_2d_pair(&tmA, bar, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
+                        tma_load_2d_pair(&tmB, bar, smB + s * kPairHalf + c * kBChunkBytes, n0 + c * 64, r0);
+                    }
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer (CTA 0 only)
+        // A segment's last K block usually holds rows of the next segment past
+        // `tail`: only its first ceil(tail/16) K steps are issued, and the rows of
+        // the last issued step past `tail` (at most 15) are zeroed in the A and B
+        // tiles of both CTAs (whole 128-byte rows, so the swizzle does not matter)
+        // before the MMAs read them.
+        const uint32_t idesc = idesc_bf16(kPairBM, kPairBN, true, true);
+        uint32_t s = 0, ph = 0;
+        bool live = lead;
+        int it = 0;
+        for (int unit = cl0; unit < total && live; unit += ncl, ++it) {
+            MTile t;
+            int mp, nt, kb_n, tail;
+            unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
+            tc_fence_after();
+            const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
+            for (int kb = 0; kb < kb_n; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, s_abort, status))) {
+                    live = false;
+                    break;
+                }
+                const bool last = kb == kb_n - 1;
+                const int ksteps = last ? (tail + 15) / 16 : kBK / 16;
+                if (last && (tail & 15)) {
+                    const int nrow = 16 - (tail & 15);
+                    const int n16 = nrow * 8 * 4;   // rows x 16-byte pieces x (2 A + 2 B chunks)
+                    for (int i = lane; i < 2 * n16; i += 32) {
+                        const int cta = i >= n16;
+                        const int j = i - cta * n16;
+                        const int piece = j & 7;
+                        const int rc = j >> 3;
+                        const int r = tail + rc % nrow;
+                        const int c = rc / nrow;
+                        uint8_t* base = c < 2 ? smA + s * kPairHalf + c * kBChunkBytes
+                                              : smB + s * kPairHalf + (c - 2) * kBChunkBytes;
+                        st_cluster_zero16(cluster_addr(base + r * 128 + piece * 16, (uint32_t)cta));
+                    }
+                    // generic-proxy stores to both CTAs become visible to the tensor core's async proxy
+                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smA + s * kPairHalf);
+                    const uint32_t b0 = smem_u32(smB + s * kPairHalf);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        if (kk < ksteps)
+                            mma_bf16_pair(dt, operand_desc<true>(a0, kk), operand_desc<true>(b0, kk), idesc,
+                                          (kb | kk) != 0);
+                    mma_commit_pair(&empty[s]);
+                }
+                __syncwarp();
+                if (++s == kPairStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (live && lane == 0) mma_commit_pair(&tfull[acc]);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs: own 128 rows)
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const int c_lo = (e / 4) * (kPairBN / 2);
+        int it = 0;
+        for (int unit = cl0; unit < total; unit += ncl, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            const bool got = mbar_wait(&tfull[acc], aph, s_abort, status);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            MTile t;
+            int mp, nt, kb_n, tail;
+            unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * acc_stride);
+            const CUtensorMap* tmO = t.wsel >= 0 ? &tmG : &tmR;
+            const int orow0 = (t.wsel >= 0 ? t.wsel : (-1 - t.wsel)) * p.H + mp * kPairBM +
+                              (int)rank * 128 + q * 32;
+            uint8_t* stg = smO + e * kOutBox;
+            uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
+            for (int c0 = c_lo; c0 < c_lo + kPairBN / 2; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    srow[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(tmO, stg, nt * kPairBN + c0, orow0);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (lead) mbar_arrive(&tempty[acc]);
+                else mbar_arrive_rank(&tempty[acc], 0);
+            }
+        }
+        if (lane == 0) bulk_wait_all();   // every reduce this warp issued has been applied
+        __syncwarp();
+    }
+
+    __syncthreads();
+    if (*s_abort) {
+        // let copies and MMAs that were already issued land before the memory goes away
+        for (int i = 0; i < 100; ++i) __nanosleep(10000);
+    }
+    cluster_sync();   // neither CTA leaves while the other may still signal it or read its tiles
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- wait self-test
 // One thread waits, through the GEMM's bounded-wait helper, on an mbarrier that
 // nothing ever arrives on. The wait gives up after timeout_ns, records
@@ -688,6 +1009,30 @@ int tmem_cols_for(int BN) {
     return c;
 }
 
+size_t pair_smem_bytes() {
+    return 1024 + (size_t)kPairStages * 2 * kPairHalf + (size_t)kPairEpiWarps * kOutBox +
+           (3 * kPairStages + 4) * 8 + 16;
+}
+
+// Clusters of two that can be resident at once, per device (0: no pair launch).
+constexpr int kMaxDevices = 64;
+int g_pair_clusters[kMaxDevices] = {};
+
+cudaLaunchConfig_t pair_config(int clusters, cudaStream_t st, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = pair_smem_bytes();
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const CUtensorMap& o0, const CUtensorMap& o1, const GemmParams& prm,
@@ -705,7 +1050,6 @@ cudaError_t launch_wait_selftest(const Workspace& ws, uint64_t timeout_ns, cudaS
 }
 
 cudaError_t gemm_setup(int device) {
-    (void)device;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -714,8 +1058,25 @@ cudaError_t gemm_setup(int device) {
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_bytes<kDx>(256));
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(grouped_gemm_kernel<kDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes<kDw>(256));
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kDw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<kDw>(256));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(grouped_gemm_dw_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)pair_smem_bytes());
+    if (err != cudaSuccess) return err;
+    // how many SM pairs can hold one pair kernel CTA each at once (0 keeps DW on single CTAs)
+    int nsm = 0;
+    err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, device);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(nsm / 2, nullptr, attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_dw_pair_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        clusters = 0;
+    }
+    if (device >= 0 && device < kMaxDevices) g_pair_clusters[device] = clusters;
+    return cudaSuccess;
 }
 
 cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -837,6 +1198,17 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = d.H / kBM;
     prm.status = ws.status;
+    // SM pairs when the tile divides the gradient: 256 x 256 tiles, six-stage rings
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const int pairs = (dev >= 0 && dev < kMaxDevices) ? g_pair_clusters[dev] : 0;
+    if (pairs > 0 && num_sms >= 2 && d.H % kPairBM == 0 && d.Hp % kPairBN == 0) {
+        prm.BN = kPairBN;
+        prm.tmem_cols = 2 * kPairBN;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_config(pairs < num_sms / 2 ? pairs : num_sms / 2, st, attr);
+        return cudaLaunchKernelEx(&cfg, grouped_gemm_dw_pair_kernel, tmA, tmB, tmG, tmR, prm);
+    }
     return launch_mode<kDw>(tmA, tmB, tmB, tmG, tmR, prm, num_sms, st);
 }
 

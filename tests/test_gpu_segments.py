@@ -43,8 +43,8 @@ def table():
     return cu
 
 
-def context(bep):
-    return bep.Context(bep.Config(R, E, B, K, S, H, HP, 0))
+def context(bep, h=H, hp=HP):
+    return bep.Context(bep.Config(R, E, B, K, S, h, hp, 0))
 
 
 def covered(cu):
@@ -110,12 +110,15 @@ def test_input_gradient_on_ragged_segments(lib):
     assert (got[~covered(cu)] == 3.0).all()
 
 
+@pytest.mark.parametrize("H, HP", [(256, 128), (512, 256)])
 @pytest.mark.parametrize("poison", [False, True])
-def test_weight_gradient_on_ragged_segments(lib, poison):
+def test_weight_gradient_on_ragged_segments(lib, poison, H, HP):
     """poison=True fills the receive rows outside every segment with +inf: a tail
-    step that read them unzeroed would turn a gradient row non-finite."""
+    step that read them unzeroed would turn a gradient row non-finite. H=512,
+    H'=256 runs the weight gradient on SM pairs (256 x 256 tiles, each CTA
+    zeroing the tail rows of its own halves); H=256, H'=128 on single CTAs."""
     bep = lib
-    ctx = context(bep)
+    ctx = context(bep, H, HP)
     cu = table()
     recv = synth.tokens_host((R * C, H), 321)
     dy = synth.tokens_host((R * C, HP), 322)
