@@ -248,8 +248,51 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_
         : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_zero16(uint32_t addr_cl) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr_cl), "r"(0) : "memory");
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait (as mbar_wait) for a barrier that the other CTA of the pair arrives on,
+// with cluster-scope acquire: what that CTA wrote before its release is visible after.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  int32_t* status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            set_status(status, BEP_DERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Zero the rows [tail, 16 * ceil(tail / 16)) of a stage's two 64-column A chunks and
+// two B chunks in this CTA's shared memory (whole 128-byte rows, so the swizzle does
+// not matter), then make the stores visible to the tensor core's async proxy. Warp-wide.
+__device__ __forceinline__ void zero_tail_rows(uint8_t* a_stage, uint8_t* b_stage, int tail, int lane) {
+    const int nrow = 16 - (tail & 15);
+    const int n16 = nrow * 8 * 4;   // rows x 16-byte pieces x (2 A + 2 B chunks)
+    for (int i = lane; i < n16; i += 32) {
+        const int piece = i & 7;
+        const int rc = i >> 3;
+        const int r = tail + rc % nrow;
+        const int c = rc / nrow;
+        uint8_t* base = c < 2 ? a_stage + c * kBChunkBytes : b_stage + (c - 2) * kBChunkBytes;
+        *reinterpret_cast<uint4*>(base + r * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
 }
 
 // One MMA of the pair: M = 256 rows, 128 from each CTA's A tile; N columns, N/2 from each
@@ -695,18 +738,28 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 // gradient exactly as the single-CTA kernel does (same tiles of 32 x 32 fp32, same
 // K order, so the sums are the same bit for bit).
 //   barriers        owner   arrivals
-//   full[s]         CTA 0   CTA 0's producer (expect_tx of both CTAs' bytes) + both CTAs' TMA bytes
+//   full[s]         CTA 0   CTA 0's producer (expect_tx) + CTA 0's TMA bytes + CTA 1's TMA bytes
+//                           (CTA 1's except in a tail stage)
+//   ptail[k % 8]    CTA 1   CTA 1's producer (expect_tx) + CTA 1's TMA bytes of the k-th tail stage
+//   zpeer[k % 8]    CTA 0   CTA 1's warp 1, once CTA 1's rows of the k-th tail stage are zero
 //   empty[s]        both    the MMA thread's multicast commit
 //   tfull[a]        both    the MMA thread's multicast commit at the end of a unit
 //   tempty[a]       CTA 0   the 8 epilogue warps of each CTA
 // CTA 1's loads count on CTA 0's full barrier, so CTA 0 knows when the whole stage
-// is in; CTA 0's MMA warp then zeroes a segment's tail rows in both CTAs' tiles
-// (CTA 1's through distributed shared memory). Every wait is bounded; the CTAs
-// meet at a cluster barrier before TMEM is freed and either exits.
+// is in. A segment's last K block usually holds rows of the next segment: in that
+// "tail stage" each CTA zeroes the extra rows of its own tiles. CTA 1 loads its tail
+// stage onto its own barrier, zeroes, and tells CTA 0 with one remote arrive per
+// unit, ahead of the MMAs that need it. The ring holds 6 stages, so at most 6 tail
+// stages are loaded and not yet consumed; 8 ptail and 8 zpeer barriers therefore
+// never see two unobserved phases, which a parity wait could not tell apart.
+// Every wait is bounded; the CTAs meet at a cluster barrier before TMEM is freed
+// and either exits.
 constexpr int kPairStages = 6;
 constexpr int kPairEpiWarps = 8;
 constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
 constexpr int kPairHalf = 2 * kBChunkBytes;   // 16 KB: one CTA's A (or B) tile of a K block
+constexpr int kPairTails = 8;                 // ptail / zpeer barriers (> stages in the ring)
+constexpr int kPairBars = 2 * kPairStages + 4 + 2 * kPairTails;
 constexpr int kPairBN = 256;
 constexpr int kPairBM = 256;
 
@@ -722,10 +775,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
     uint8_t* smO = smB + kPairStages * kPairHalf;   // a 4 KB staging box per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smO + kPairEpiWarps * kOutBox);
     uint64_t* full = bars;
-    uint64_t* empty = bars + 2 * kPairStages;
-    uint64_t* tfull = bars + 3 * kPairStages;
-    uint64_t* tempty = bars + 3 * kPairStages + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * kPairStages + 4);
+    uint64_t* empty = bars + kPairStages;
+    uint64_t* tfull = bars + 2 * kPairStages;
+    uint64_t* tempty = bars + 2 * kPairStages + 2;
+    uint64_t* ptail = bars + 2 * kPairStages + 4;
+    uint64_t* zpeer = ptail + kPairTails;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kPairBars);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int32_t* status = p.status;
     const uint32_t rank = cluster_rank();
@@ -740,6 +795,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 2 * kPairEpiWarps);
+        }
+        for (int k = 0; k < kPairTails; ++k) {
+            mbar_init(&ptail[k], 1);
+            mbar_init(&zpeer[k], 1);
         }
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -777,7 +836,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (each CTA its own half)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-            uint32_t s = 0, ph = 0;
+            uint32_t s = 0, ph = 0, tk = 0;
             bool live = true;
             for (int unit = cl0; unit < total && live; unit += ncl) {
                 MTile t;
@@ -790,13 +849,24 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                         live = false;
                         break;
                     }
-                    // CTA 0's barrier counts both CTAs' 32 KB
-                    if (lead) mbar_arrive_expect_tx(&full[s], 4 * kPairHalf);
-                    const uint32_t bar = cluster_addr(&full[s], 0);
+                    // CTA 0's barrier counts both CTAs' 32 KB, except that CTA 1's tail
+                    // stage counts on CTA 1's own barrier
+                    const bool tstage = kb == kb_n - 1 && (tail & 15);
                     const int r0 = t.row0 + kb * kBK;
-                    for (int c = 0; c < 2; ++c) {
-                        tma_load_2d_pair(&tmA, bar, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
-                        tma_load_2d_pair(&tmB, bar, smB + s * kPairHalf + c * kBChunkBytes, n0 + c * 64, r0);
+                    if (!lead && tstage) {
+                        uint64_t* tb = &ptail[tk++ % kPairTails];
+                        mbar_arrive_expect_tx(tb, 2 * kPairHalf);
+                        for (int c = 0; c < 2; ++c) {
+                            tma_load_2d(&tmA, tb, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
+                            tma_load_2d(&tmB, tb, smB + s * kPairHalf + c * kBChunkBytes, n0 + c * 64, r0);
+                        }
+                    } else {
+                        if (lead) mbar_arrive_expect_tx(&full[s], (tstage ? 2 : 4) * kPairHalf);
+                        const uint32_t bar = cluster_addr(&full[s], 0);
+                        for (int c = 0; c < 2; ++c) {
+                            tma_load_2d_pair(&tmA, bar, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
+                            tma_load_2d_pair(&tmB, bar, smB + s * kPairHalf + c * kBChunkBytes, n0 + c * 64, r0);
+                        }
                     }
                     if (++s == kPairStages) {
                         s = 0;
@@ -806,68 +876,78 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------- MMA issuer (CTA 0 only)
+        // ---------------------------------------------------- CTA 0: MMA issuer; CTA 1: tail rows
         // A segment's last K block usually holds rows of the next segment past
         // `tail`: only its first ceil(tail/16) K steps are issued, and the rows of
         // the last issued step past `tail` (at most 15) are zeroed in the A and B
-        // tiles of both CTAs (whole 128-byte rows, so the swizzle does not matter)
-        // before the MMAs read them.
-        const uint32_t idesc = idesc_bf16(kPairBM, kPairBN, true, true);
-        uint32_t s = 0, ph = 0;
-        bool live = lead;
-        int it = 0;
-        for (int unit = cl0; unit < total && live; unit += ncl, ++it) {
-            MTile t;
-            int mp, nt, kb_n, tail;
-            unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
-            const int acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
-            tc_fence_after();
-            const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
-            for (int kb = 0; kb < kb_n; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, s_abort, status))) {
-                    live = false;
-                    break;
-                }
-                const bool last = kb == kb_n - 1;
-                const int ksteps = last ? (tail + 15) / 16 : kBK / 16;
-                if (last && (tail & 15)) {
-                    const int nrow = 16 - (tail & 15);
-                    const int n16 = nrow * 8 * 4;   // rows x 16-byte pieces x (2 A + 2 B chunks)
-                    for (int i = lane; i < 2 * n16; i += 32) {
-                        const int cta = i >= n16;
-                        const int j = i - cta * n16;
-                        const int piece = j & 7;
-                        const int rc = j >> 3;
-                        const int r = tail + rc % nrow;
-                        const int c = rc / nrow;
-                        uint8_t* base = c < 2 ? smA + s * kPairHalf + c * kBChunkBytes
-                                              : smB + s * kPairHalf + (c - 2) * kBChunkBytes;
-                        st_cluster_zero16(cluster_addr(base + r * 128 + piece * 16, (uint32_t)cta));
+        // tiles of both CTAs before the MMAs read them, each CTA its own.
+        if (lead) {
+            const uint32_t idesc = idesc_bf16(kPairBM, kPairBN, true, true);
+            uint32_t s = 0, ph = 0, zc = 0;
+            bool live = true;
+            int it = 0;
+            for (int unit = cl0; unit < total && live; unit += ncl, ++it) {
+                MTile t;
+                int mp, nt, kb_n, tail;
+                unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
+                const int acc = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
+                for (int kb = 0; kb < kb_n; ++kb) {
+                    const bool last = kb == kb_n - 1;
+                    const bool tstage = last && (tail & 15);
+                    bool ok = mbar_wait(&full[s], ph, s_abort, status);
+                    if (ok && tstage)
+                        ok = mbar_wait_cluster(&zpeer[zc % kPairTails], (zc / kPairTails) & 1u, s_abort, status);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        live = false;
+                        break;
                     }
-                    // generic-proxy stores to both CTAs become visible to the tensor core's async proxy
-                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(smA + s * kPairHalf);
-                    const uint32_t b0 = smem_u32(smB + s * kPairHalf);
+                    if (tstage) {
+                        ++zc;
+                        zero_tail_rows(smA + s * kPairHalf, smB + s * kPairHalf, tail, lane);
+                    }
+                    const int ksteps = last ? (tail + 15) / 16 : kBK / 16;
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(smA + s * kPairHalf);
+                        const uint32_t b0 = smem_u32(smB + s * kPairHalf);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        if (kk < ksteps)
-                            mma_bf16_pair(dt, operand_desc<true>(a0, kk), operand_desc<true>(b0, kk), idesc,
-                                          (kb | kk) != 0);
-                    mma_commit_pair(&empty[s]);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            if (kk < ksteps)
+                                mma_bf16_pair(dt, operand_desc<true>(a0, kk), operand_desc<true>(b0, kk), idesc,
+                                              (kb | kk) != 0);
+                        mma_commit_pair(&empty[s]);
+                    }
+                    __syncwarp();
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                __syncwarp();
-                if (++s == kPairStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                if (live && lane == 0) mma_commit_pair(&tfull[acc]);
             }
-            if (live && lane == 0) mma_commit_pair(&tfull[acc]);
+        } else {
+            // CTA 1: follow the stage sequence; in each unit's tail stage wait for the
+            // own bytes, zero the tail rows and release the stage to CTA 0's MMA thread
+            uint32_t s = 0, tc = 0;
+            for (int unit = cl0; unit < total; unit += ncl) {
+                MTile t;
+                int mp, nt, kb_n, tail;
+                unit_of(unit, &t, &mp, &nt, &kb_n, &tail);
+                const uint32_t st = (s + (uint32_t)kb_n - 1) % kPairStages;
+                s = (s + (uint32_t)kb_n) % kPairStages;
+                if (!(tail & 15)) continue;
+                if (!__all_sync(0xffffffffu, mbar_wait(&ptail[tc % kPairTails], (tc / kPairTails) & 1u,
+                                                       s_abort, status)))
+                    break;
+                zero_tail_rows(smA + st * kPairHalf, smB + st * kPairHalf, tail, lane);
+                if (lane == 0) mbar_arrive_rank(&zpeer[tc % kPairTails], 0);
+                ++tc;
+                __syncwarp();
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue (both CTAs: own 128 rows)
@@ -1010,8 +1090,7 @@ int tmem_cols_for(int BN) {
 }
 
 size_t pair_smem_bytes() {
-    return 1024 + (size_t)kPairStages * 2 * kPairHalf + (size_t)kPairEpiWarps * kOutBox +
-           (3 * kPairStages + 4) * 8 + 16;
+    return 1024 + (size_t)kPairStages * 2 * kPairHalf + (size_t)kPairEpiWarps * kOutBox + kPairBars * 8 + 16;
 }
 
 // Clusters of two that can be resident at once, per device (0: no pair launch).
