@@ -341,7 +341,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- work list
-// seg_mode == 0: m-tiles of <= 128 rows per non-empty segment (FWD, DX);
+// Exclusive scan of one int per thread over the block; *total gets the sum.
+// Every thread of the block must call it (it synchronises).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __syncthreads();   // s_warp may still be read by a previous call
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < nwarps ? s_warp[lane] : 0;
+        int wi = w;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        if (lane < nwarps) s_warp[lane] = wi - w;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    *total = s_warp[32];
+    return s_warp[warp] + incl - v;
+}
+
+// seg_mode == 0: m-tiles of <= 128 rows per non-empty segment (FWD, DX). The tiles
+//   of segments with three or more m-tiles ("long": after their first tile the
+//   weight row is in L2, so they are tensor-bound) and of shorter segments
+//   ("short": their tiles mostly stream a whole weight row, HBM-bound) form two lists, each in
+//   (rank, row) order, merged evenly so that both kinds run side by side. A long
+//   segment's tiles keep their order, with at most a few short tiles between two
+//   of them. With every segment long (training sizes) the order is plain
+//   (rank, row, m).
 // seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
@@ -362,35 +396,29 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         if (seg_mode) return b > a ? 1 : 0;
         return (b - a + kBM - 1) / kBM;
     };
-    int sum = 0;
+    int nlong = 0, nshort = 0;
     for (int i = lo; i < hi; ++i) {
         int s, l;
-        sum += tiles_of(i, &s, &l);
+        const int n = tiles_of(i, &s, &l);
+        if (n > 2) nlong += n;
+        else nshort += n;
     }
-    // block exclusive scan
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    int incl = sum;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int w = lane < nwarps ? s_warp[lane] : 0;
-        int wi = w;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += n;
-        }
-        if (lane < nwarps) s_warp[lane] = wi - w;
-        if (lane == 31) s_warp[32] = wi;
-    }
-    __syncthreads();
-    int run = s_warp[warp] + incl - sum;
-    const int total = s_warp[32];
+    int Nl = 0, Ns = 0;
+    int run_l = block_exclusive_scan(nlong, s_warp, &Nl);
+    int run_s = block_exclusive_scan(nshort, s_warp, &Ns);
+    const int total = Nl + Ns;
     // one inconsistent segment anywhere refuses the whole table: nothing is computed
     const bool ok = !__syncthreads_or(bad) && total <= d.max_tiles;
+    // merged position of the k-th long tile / k-th short tile: order by the stamps
+    // (2k+1)/(2 Nl) and (2k+1)/(2 Ns), a long tile first on a tie
+    auto pos_long = [&](int k) -> int {
+        const int64_t q = ((2 * (int64_t)k + 1) * Ns + Nl - 1) / Nl;
+        return k + (int)(q / 2 < Ns ? q / 2 : Ns);
+    };
+    auto pos_short = [&](int k) -> int {
+        const int64_t y = ((2 * (int64_t)k + 1) * Nl) / Ns;
+        return k + (int)((y + 1) / 2 < Nl ? (y + 1) / 2 : Nl);
+    };
     for (int i = lo; i < hi && ok; ++i) {
         int s = 0, l = 0;
         const int n = tiles_of(i, &s, &l);
@@ -402,9 +430,11 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             t.rows = seg_mode ? l : min(kBM, l - m * kBM);
             t.wsel = wsel;
             t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
-            ws.tiles[run + m] = t;
+            const int at = seg_mode ? run_s + m : (n > 2 ? pos_long(run_l + m) : pos_short(run_s + m));
+            ws.tiles[at] = t;
         }
-        run += n;
+        if (n > 2) run_l += n;
+        else run_s += n;
     }
     if (threadIdx.x == 0) {
         if (!ok) set_status(ws.status, BEP_DERR_BOUNDS);
