@@ -374,8 +374,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   ("short": their tiles mostly stream a whole weight row, HBM-bound) form two lists, each in
 //   (rank, row) order, merged evenly so that both kinds run side by side. A long
 //   segment's tiles keep their order, with at most a few short tiles between two
-//   of them. With every segment long (training sizes) the order is plain
-//   (rank, row, m).
+//   of them. At training sizes nearly every segment is long; the few short ones
+//   (small replica pieces) are spread among the rest.
 // seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
@@ -411,12 +411,17 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
     const bool ok = !__syncthreads_or(bad) && total <= d.max_tiles;
     // merged position of the k-th long tile / k-th short tile: order by the stamps
     // (2k+1)/(2 Nl) and (2k+1)/(2 Ns), a long tile first on a tie
+    // (32-bit division when the products fit, as they do below ~46k tiles)
+    const bool narrow = (int64_t)(2 * total + 1) * total < (int64_t)UINT32_MAX;
+    auto div = [&](int64_t a, int b) -> int64_t {
+        return narrow ? (int64_t)((uint32_t)a / (uint32_t)b) : a / b;
+    };
     auto pos_long = [&](int k) -> int {
-        const int64_t q = ((2 * (int64_t)k + 1) * Ns + Nl - 1) / Nl;
+        const int64_t q = div((2 * (int64_t)k + 1) * Ns + Nl - 1, Nl);
         return k + (int)(q / 2 < Ns ? q / 2 : Ns);
     };
     auto pos_short = [&](int k) -> int {
-        const int64_t y = ((2 * (int64_t)k + 1) * Nl) / Ns;
+        const int64_t y = div((2 * (int64_t)k + 1) * Nl, Ns);
         return k + (int)((y + 1) / 2 < Nl ? (y + 1) / 2 : Nl);
     };
     for (int i = lo; i < hi && ok; ++i) {
@@ -430,7 +435,10 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             t.rows = seg_mode ? l : min(kBM, l - m * kBM);
             t.wsel = wsel;
             t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
-            const int at = seg_mode ? run_s + m : (n > 2 ? pos_long(run_l + m) : pos_short(run_s + m));
+            const int at = (seg_mode || Nl == 0) ? run_s + m
+                           : Ns == 0               ? run_l + m
+                           : n > 2                 ? pos_long(run_l + m)
+                                                   : pos_short(run_s + m);
             ws.tiles[at] = t;
         }
         if (n > 2) run_l += n;
