@@ -172,6 +172,83 @@ def run_inference(bep, synth, w_home, stream, dev, reps):
     return res
 
 
+def run_small_configs(bep, synth, stream, dev, reps):
+    """Latency of every stage at the small workloads, whose inputs fit in L2: the tiny
+    one (R=2, E=8), the E=64 training workload at each of its maxvio targets, and the
+    reduce_grad workload (H=2048, H'=1024, replica gradients N(0, 1e-3) in the used
+    slots, then combine backward on H-wide rows). A 256 MiB buffer is written before
+    every repeat so that no stage starts with its inputs in L2. Median microseconds."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {"l2_flush": "256 MiB written before every repeat (L2 is 126 MiB)", "unit": "us"}
+
+    def timed(fns, n):
+        times = {k: [] for k in fns}
+        for _ in range(n + 1):
+            for k, fn in fns.items():
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                times[k].append((a, b))
+        torch.cuda.synchronize()
+        return {k: round(statistics.median(a.elapsed_time(b) for a, b in v[1:]) * 1e3, 1)
+                for k, v in times.items()}
+
+    for name in ("tiny_r2_e8", "train_r8_e64", "grad_r8_e64"):
+        wl = synth.WORKLOADS[name]
+        R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
+        cfg = bep.Config(R, E, B, K, S, H, Hp, wl.mode)
+        ctx = bep.Context(cfg)
+        buf = bep.Buffers(cfg, dev, with_grad=True)
+        x = synth.tokens_device((R, S, H), 21, device=dev)
+        gates = torch.from_numpy(synth.gates_host(R, S, K, 21)).to(dev)
+        dout = synth.tokens_device((R, S, Hp), 22, device=dev)
+        w_home = synth.weights_device((E, H, Hp), 23, device=dev)
+        w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=dev)
+        res = {"workload": f"{name} (R={R}, S={S}/rank, E={E}, K={K}, H={H}, H'={Hp}, B={B})"}
+        for target in synth.MAXVIO_TARGETS[name]:
+            topk = torch.from_numpy(synth.routing(wl, target, 0)).to(dev)
+            key = "zipf1.2" if target is None else f"{target:g}"
+            if name == "grad_r8_e64":
+                # the backward fold: reduce_grad on the replica gradients, combine backward on
+                # the [S*K, H] receive rows
+                bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
+                g = torch.zeros((E, H, Hp), dtype=torch.float32, device=dev)
+                red = torch.empty((R, B, H, Hp), dtype=torch.float32, device=dev).normal_(0, 1e-3)
+                dout_h = synth.tokens_device((R, S, H), 24, device=dev)
+                dy_h = torch.empty((R * S * K, H), dtype=torch.bfloat16, device=dev)
+                fns = {"reduce_grad": lambda: bep.bep_reduce_grad(ctx, buf.slot_expert, g, red, stream),
+                       "combine_bwd_d_h": lambda: bep.bep_combine_bwd(ctx, dout_h, buf.dest, gates, dy_h,
+                                                                      stream)}
+                res[key] = timed(fns, reps)
+                res[key]["replicas"] = int((buf.slot_expert >= 0).sum().item())
+                del g, red, dout_h, dy_h
+                continue
+            fns = {
+                "plan": lambda: bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest,
+                                             buf.maxvio, stream),
+                "prefetch": lambda: bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream),
+                "dispatch": lambda: bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream),
+                "gemm": lambda: bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots,
+                                                     buf.y, stream),
+                "combine": lambda: bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream),
+                "combine_bwd": lambda: bep.bep_combine_bwd(ctx, dout, buf.dest, gates, buf.dy, stream),
+            }
+            res[key] = timed(fns, reps)
+            res[key]["maxvio"] = round(float(buf.maxvio.item()), 4)
+        st = bep.bep_status(ctx, stream)
+        if st:
+            raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+        out[name] = res
+        del ctx, buf, x, gates, dout, w_home, w_slots
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
@@ -366,6 +443,11 @@ def run_gpu(args, rank, world, local_rank):
     infer = None
     if not args.no_backward and args.workload == WORKLOAD:
         infer = run_inference(bep, synth, w_home, stream, dev, min(args.steps, 8))
+
+    # ---- the small workloads (inputs fit in L2): per-stage latency with L2 flushed
+    small = None
+    if not args.no_backward and args.workload == WORKLOAD:
+        small = run_small_configs(bep, synth, stream, dev, 9)
 
     # ---- the second projection: the down projection [E+B, H', H] on the same plan (a second
     # context with H and H' swapped), fed by the first projection's output rows
@@ -585,6 +667,7 @@ def run_gpu(args, rank, world, local_rank):
         "combine_d_h": comb_h,
         "second_projection": proj2,
         "inference": infer,
+        "small_configs": small,
     }
     return result
 

@@ -149,3 +149,46 @@ def test_weight_gradient_on_ragged_segments(lib, poison, H, HP):
                 continue
             err = np.linalg.norm(rh[u, j] - (red0[u, j] + d_slots[u, j])) / np.linalg.norm(d_slots[u, j])
             assert err <= RTOL, (u, j, err)
+
+
+def test_weight_gradient_on_many_tiny_segments_sm_pairs(lib):
+    """dW on SM pairs (H=512, H'=256) over random tables where most segments hold
+    1-15 rows: long runs of units that are a single tail block each, so up to the
+    ring's six tail stages are in flight at once and every tail barrier is reused
+    many times. Compared per weight row with the binary64 oracle."""
+    bep = lib
+    R_, E_, B_, K_, S_, H_, HP_ = 4, 64, 16, 4, 96, 512, 256
+    C_ = S_ * K_
+    rng = np.random.default_rng(17)
+    cu = np.zeros((R_, E_ + B_ + 1), np.int32)
+    for u in range(R_):
+        lens = rng.choice([0, 1, 2, 3, 5, 7, 9, 12, 15, 17, 33], size=E_ + B_,
+                          p=[.2, .15, .1, .1, .1, .1, .05, .05, .05, .05, .05])
+        while lens.sum() > C_:
+            lens[rng.integers(E_ + B_)] //= 2
+        cu[u, 1:] = np.cumsum(lens)
+    ctx = bep.Context(bep.Config(R_, E_, B_, K_, S_, H_, HP_, 0))
+    recv = synth.tokens_host((R_ * C_, H_), 331)
+    dy = synth.tokens_host((R_ * C_, HP_), 332)
+    g0 = synth.normal_host((E_, H_, HP_), 333, 0.5)
+    red0 = synth.normal_host((R_, B_, H_, HP_), 334, 0.5)
+    g = torch.from_numpy(g0).to(DEV)
+    red = torch.from_numpy(red0).to(DEV)
+    bep.bep_grouped_gemm_dw(ctx, torch.from_numpy(cu).to(DEV), dev_u16(recv), dev_u16(dy), g, red)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    d_home, d_slots = oracle.grouped_gemm_dw(recv, dy, cu, E_, B_, H_, HP_)
+    gh, rh = g.cpu().numpy().astype(np.float64), red.cpu().numpy().astype(np.float64)
+    for e in range(E_):
+        if not d_home[e].any():
+            np.testing.assert_array_equal(gh[e], g0[e])
+            continue
+        err = np.linalg.norm(gh[e] - (g0[e] + d_home[e])) / np.linalg.norm(d_home[e])
+        assert err <= RTOL, (e, err)
+    for u in range(R_):
+        for j in range(B_):
+            if not d_slots[u, j].any():
+                np.testing.assert_array_equal(rh[u, j], red0[u, j])
+                continue
+            err = np.linalg.norm(rh[u, j] - (red0[u, j] + d_slots[u, j])) / np.linalg.norm(d_slots[u, j])
+            assert err <= RTOL, (u, j, err)
