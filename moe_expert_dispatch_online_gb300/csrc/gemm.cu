@@ -60,7 +60,7 @@ struct ModeCfg {
     static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
     static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
     static constexpr int kStages = 4;
-    static constexpr int kOutBufs = 1;                     // staging boxes per epilogue warp
+    static constexpr int kOutBufs = MODE == kDw ? 1 : 2;   // staging boxes per epilogue warp
     static constexpr int kWarps = 2 + kEpiWarps;
     static constexpr int kThreads = 32 * kWarps;
 };
@@ -138,6 +138,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
         "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
         ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
         : "memory");
+}
+// Plain copy of a shared-memory box into global memory (the box's rows must all lie
+// inside the destination); completion is tracked per issuing thread with bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -669,6 +679,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         const int cspan = BN / halves;
         const int c_lo = (e / 4) * cspan;
         int it = 0;
+        int obox = 0, last_store = -1;   // FWD/DX: next staging box; box of the newest TMA store
         for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -709,15 +720,28 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             } else {
                 // 64 columns at a time: round to bf16 (nearest even) and stage the warp's
                 // 32 rows x 128 B in shared memory (16-byte piece j of row r sits at
-                // j ^ (r & 7)); read them back a row per 8 lanes so that each store
-                // instruction writes four whole 128-byte lines. Rows past the segment end
-                // belong to the next segment's tile and are skipped.
+                // j ^ (r & 7), the 128-byte swizzle). A box whose 32 rows all lie inside
+                // the segment leaves by one TMA store; a segment's ragged last box is read
+                // back a row per 8 lanes and stored by the threads (each instruction writes
+                // four whole 128-byte lines), skipping the rows past the segment end, which
+                // belong to the next segment's tile. Two boxes per warp alternate, so one
+                // store can be in flight while the next box is filled.
                 const int nvalid = u.t.rows - q * 32;   // this warp's rows inside the segment
-                uint8_t* stg = smO + e * kOutBox;
-                uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
                 const int rsub = lane >> 3, piece = lane & 7;
-                uint16_t* ybase = p.out + ((int64_t)u.t.row0 + q * 32) * p.N + (int64_t)u.nt * BN;
+                const int orow = u.t.row0 + q * 32;
+                uint16_t* ybase = p.out + (int64_t)orow * p.N + (int64_t)u.nt * BN;
                 for (int c0 = c_lo; c0 < c_lo + cspan && nvalid > 0; c0 += 64) {
+                    const int b = obox++ & 1;
+                    uint8_t* stg = smO + (e * CF::kOutBufs + b) * kOutBox;
+                    uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
+                    // a store issued from this box earlier has read it: every bulk group but the
+                    // newest is complete after wait_group.read 1; if the newest came from this box
+                    // too, wait for it as well
+                    if (lane == 0) {
+                        if (last_store == b) bulk_wait_read_all();
+                        else bulk_wait_read_1();
+                    }
+                    __syncwarp();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t r[32];
@@ -732,23 +756,34 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                             srow[(4 * h + v) ^ (lane & 7)] = o;
                         }
                     }
-                    __syncwarp();
+                    if (nvalid >= 32) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmO0, stg, u.nt * BN + c0, orow);
+                            bulk_commit();
+                        }
+                        last_store = b;
+                    } else {
+                        __syncwarp();
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int rr = 4 * k + rsub;
-                        const uint4 o = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
-                        if (rr < nvalid)
-                            *reinterpret_cast<uint4*>(ybase + (int64_t)rr * p.N + c0 + piece * 8) = o;
+                        for (int k = 0; k < 8; ++k) {
+                            const int rr = 4 * k + rsub;
+                            const uint4 o =
+                                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((piece ^ (rr & 7)) << 4));
+                            if (rr < nvalid)
+                                *reinterpret_cast<uint4*>(ybase + (int64_t)rr * p.N + c0 + piece * 8) = o;
+                        }
+                        __syncwarp();   // the box is read back before it is filled again
                     }
-                    __syncwarp();   // the box is read back before the next chunk overwrites it
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
         }
-        // DW: every reduce this warp issued has been applied before the CTA ends
-        if (MODE == kDw && lane == 0) bulk_wait_all();
+        // every store or reduce this warp issued has completed before the CTA ends
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
@@ -1214,6 +1249,8 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     GemmParams prm = {};
     prm.tiles = ws.tiles;
     prm.ntiles = ws.ntiles;
+    CUtensorMap tmY;   // Y [R*C, H'] in 32-row x 64-column boxes: the epilogue's stores
+    if (!encode_2d(&tmY, y, (uint64_t)d.R * d.C, d.Hp, 32, 64)) return cudaErrorInvalidValue;
     prm.out = y;
     prm.N = d.Hp;
     prm.Kdim = d.H;
@@ -1222,7 +1259,7 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = 1;
     prm.status = ws.status;
-    return launch_mode<kFwd>(tmA, tmBh, tmBs, tmA, tmA, prm, num_sms, st);
+    return launch_mode<kFwd>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
 }
 
 // The pages' "VM group GEMM": every rank's weights are one contiguous [E+B, H, H']
@@ -1253,7 +1290,9 @@ cudaError_t launch_grouped_gemm_vm(const Dims& d, const Workspace& ws, const int
     prm.mtd = 1;
     prm.vm = 1;
     prm.status = ws.status;
-    return launch_mode<kFwd>(tmA, tmV, tmV, tmA, tmA, prm, num_sms, st);
+    CUtensorMap tmY;
+    if (!encode_2d(&tmY, y, (uint64_t)d.R * d.C, d.Hp, 32, 64)) return cudaErrorInvalidValue;
+    return launch_mode<kFwd>(tmA, tmV, tmV, tmY, tmY, prm, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int32_t* cu,
@@ -1275,6 +1314,8 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
     GemmParams prm = {};
     prm.tiles = ws.tiles;
     prm.ntiles = ws.ntiles;
+    CUtensorMap tmY;   // dRecv [R*C, H] in 32-row x 64-column boxes
+    if (!encode_2d(&tmY, drecv, (uint64_t)d.R * d.C, d.H, 32, 64)) return cudaErrorInvalidValue;
     prm.out = drecv;
     prm.N = d.H;
     prm.Kdim = d.Hp;
@@ -1283,7 +1324,7 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = 1;
     prm.status = ws.status;
-    return launch_mode<kDx>(tmA, tmBh, tmBs, tmA, tmA, prm, num_sms, st);
+    return launch_mode<kDx>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
