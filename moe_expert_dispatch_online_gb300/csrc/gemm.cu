@@ -382,10 +382,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   of segments with three or more m-tiles ("long": after their first tile the
 //   weight row is in L2, so they are tensor-bound) and of shorter segments
 //   ("short": their tiles mostly stream a whole weight row, HBM-bound) form two lists, each in
-//   (rank, row) order, merged evenly so that both kinds run side by side. A long
+//   (rank, row) order, merged evenly so that both kinds run side by side, when the
+//   short tiles are a fifth or more of all tiles (skewed inference batches). A long
 //   segment's tiles keep their order, with at most a few short tiles between two
-//   of them. At training sizes nearly every segment is long; the few short ones
-//   (small replica pieces) are spread among the rest.
+//   of them. Otherwise (training sizes: a few short segments among many long ones)
+//   the order is plain (rank, row, m).
 // seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
@@ -417,6 +418,10 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
     int run_l = block_exclusive_scan(nlong, s_warp, &Nl);
     int run_s = block_exclusive_scan(nshort, s_warp, &Ns);
     const int total = Nl + Ns;
+    // merge only where the short tiles are a fifth or more of the work (skewed inference
+    // batches); with a few short tiles among many long ones (training) spreading them
+    // only moved weight rows out of L2 early, so the order stays plain
+    const bool mix = Nl > 0 && Ns > 0 && 4 * (int64_t)Ns >= Nl;
     // one inconsistent segment anywhere refuses the whole table: nothing is computed
     const bool ok = !__syncthreads_or(bad) && total <= d.max_tiles;
     // merged position of the k-th long tile / k-th short tile: order by the stamps
@@ -445,10 +450,11 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             t.rows = seg_mode ? l : min(kBM, l - m * kBM);
             t.wsel = wsel;
             t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
-            const int at = (seg_mode || Nl == 0) ? run_s + m
-                           : Ns == 0               ? run_l + m
-                           : n > 2                 ? pos_long(run_l + m)
-                                                   : pos_short(run_s + m);
+            // plain (rank, row, m) order: the position among all tiles of this thread's range
+            const int plain = run_l + run_s + m;
+            const int at = (seg_mode || !mix) ? plain
+                           : n > 2            ? pos_long(run_l + m)
+                                              : pos_short(run_s + m);
             ws.tiles[at] = t;
         }
         if (n > 2) run_l += n;
