@@ -45,9 +45,13 @@ def draw(seed):
     H = 64 * int(rng.choice([1, 2, 3, 4, 8, 12]))
     Hp = 64 * int(rng.choice([1, 2, 3, 4, 8]))
     mode = 1 if (G >= 2 and rng.random() < 0.35) else 0
-    B = int(rng.integers(1, G)) if mode == 1 else G
+    B = (1 if rng.random() < 0.5 else int(rng.integers(1, G))) if mode == 1 else G
     alpha = float(rng.choice([0.3, 1.0, 10.0]))
     pop = rng.dirichlet(np.full(E, alpha))
+    if mode == 1 and rng.random() < 0.7:
+        # equally hot experts on home group 0: the ranks it feeds need more of its experts
+        # than they have slots, and the rest overflow onto the home rows
+        pop[:G] = 200.0 * pop.sum() / E
     pop = np.maximum(pop, 1e-9)
     topk = synth.gumbel_topk(R, S, K, pop / pop.sum(), 2000 + seed)
     return dict(R=R, E=E, B=B, K=K, S=S, H=H, Hp=Hp, mode=mode), topk
