@@ -63,8 +63,32 @@ def rel(got, ref):
 
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_whole_chain_on_random_config(lib, seed):
-    bep = lib
     c, topk = draw(seed)
+    run_chain(lib, c, topk, seed)
+
+
+# Near the library's limits (R <= 64, E <= 2048, K <= 32): many ranks, thousands of
+# experts, a wide top-K, and an inference batch whose hot group forces overflow rows.
+LIMIT_CASES = [
+    dict(R=64, E=2048, B=32, K=32, S=8, H=64, Hp=64, mode=0),
+    dict(R=16, E=512, B=32, K=16, S=32, H=128, Hp=128, mode=0),
+    dict(R=16, E=512, B=2, K=16, S=32, H=128, Hp=64, mode=1),
+]
+
+
+@pytest.mark.parametrize("case", range(len(LIMIT_CASES)))
+def test_whole_chain_near_size_limits(lib, case):
+    c = LIMIT_CASES[case]
+    G = c["E"] // c["R"]
+    rng = np.random.default_rng(77 + case)
+    pop = rng.dirichlet(np.full(c["E"], 0.5))
+    if c["mode"] == 1:
+        pop[:G] = 200.0 * pop.sum() / c["E"]
+    topk = synth.gumbel_topk(c["R"], c["S"], c["K"], pop / pop.sum(), 3000 + case)
+    run_chain(lib, c, topk, 100 + case)
+
+
+def run_chain(bep, c, topk, seed):
     R, E, B, K, S, H, Hp, mode = (c[k] for k in ("R", "E", "B", "K", "S", "H", "Hp", "mode"))
     C = S * K
     ref = oracle.plan(topk, E, B, mode)
