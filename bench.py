@@ -444,6 +444,27 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_backward and args.workload == WORKLOAD:
         infer = run_inference(bep, synth, w_home, stream, dev, min(args.steps, 8))
 
+    # ---- the ceiling of dispatch's access pattern: the same kernel with each token's K
+    # copies going to K consecutive receive rows (dest[t, k] = t*K + k, no scatter), so the
+    # time is the read-once / write-K-times pattern itself
+    fan = None
+    if not args.no_backward and args.workload == WORKLOAD:
+        dest_seq = torch.arange(R * S * K, dtype=torch.int32, device=dev).view(R, S, K)
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(6)]
+        for i in range(7):
+            if i > 0:
+                fev[i - 1][0].record(stream)
+            bep.bep_dispatch(ctx, x, dest_seq, buf.recv, stream)
+            if i > 0:
+                fev[i - 1][1].record(stream)
+        torch.cuda.synchronize()
+        fan_ms = statistics.median(e[0].elapsed_time(e[1]) for e in fev)
+        fan_bytes = R * S * H * 2 * (1 + K) + R * S * K * 4
+        fan = {"dispatch_contiguous_dest_ms": fan_ms,
+               "dispatch_contiguous_dest_gbs": fan_bytes / (fan_ms * 1e-3) / 1e9,
+               "planned_over_contiguous": statistics.mean(stage_ms["dispatch"]) / fan_ms}
+        del dest_seq
+
     # ---- the small workloads (inputs fit in L2): per-stage latency with L2 flushed
     small = None
     if not args.no_backward and args.workload == WORKLOAD:
@@ -668,6 +689,7 @@ def run_gpu(args, rank, world, local_rank):
         "second_projection": proj2,
         "inference": infer,
         "small_configs": small,
+        "dispatch_pattern_ceiling": fan,
     }
     return result
 
