@@ -446,7 +446,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---- the ceiling of dispatch's access pattern: the same kernel with each token's K
     # copies going to K consecutive receive rows (dest[t, k] = t*K + k, no scatter), so the
-    # time is the read-once / write-K-times pattern itself
+    # time is the read-once / write-K-times pattern itself; likewise for combine backward
     fan = None
     if not args.no_backward and args.workload == WORKLOAD:
         dest_seq = torch.arange(R * S * K, dtype=torch.int32, device=dev).view(R, S, K)
@@ -459,10 +459,23 @@ def run_gpu(args, rank, world, local_rank):
                 fev[i - 1][1].record(stream)
         torch.cuda.synchronize()
         fan_ms = statistics.median(e[0].elapsed_time(e[1]) for e in fev)
+        # combine backward has the same shape of traffic on H'-wide rows
+        for i in range(7):
+            if i > 0:
+                fev[i - 1][0].record(stream)
+            bep.bep_combine_bwd(ctx, dout, dest_seq, gates, buf.dy, stream)
+            if i > 0:
+                fev[i - 1][1].record(stream)
+        torch.cuda.synchronize()
+        cb_ms = statistics.median(e[0].elapsed_time(e[1]) for e in fev)
         fan_bytes = R * S * H * 2 * (1 + K) + R * S * K * 4
+        cb_bytes = R * S * Hp * 2 * (1 + K) + R * S * K * 8
         fan = {"dispatch_contiguous_dest_ms": fan_ms,
                "dispatch_contiguous_dest_gbs": fan_bytes / (fan_ms * 1e-3) / 1e9,
-               "planned_over_contiguous": statistics.mean(stage_ms["dispatch"]) / fan_ms}
+               "planned_over_contiguous": statistics.mean(stage_ms["dispatch"]) / fan_ms,
+               "combine_bwd_contiguous_dest_ms": cb_ms,
+               "combine_bwd_contiguous_dest_gbs": cb_bytes / (cb_ms * 1e-3) / 1e9,
+               "combine_bwd_planned_over_contiguous": statistics.mean(stage_ms["combine_bwd"]) / cb_ms}
         del dest_seq
 
     # ---- the small workloads (inputs fit in L2): per-stage latency with L2 flushed
