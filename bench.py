@@ -42,6 +42,12 @@ GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 25.14e9}
 # ahead of compute (1.5 GB per set at the S=8192, E=384 workload, 18 GB in all).
 E2E_DEPTH = 12
 
+# Steps the end-to-end loop times at least (about 1.5 s at the S=8192, E=384 workload).
+# Host-to-device copies on this platform stall for 40-90 ms now and then; the look-ahead
+# hides a stall in mid-run, and a longer run keeps one that falls on the first uploads,
+# which nothing can overlap, from weighing as much as it does in a 0.5 s run.
+E2E_MIN_STEPS = 120
+
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -612,7 +618,8 @@ def run_gpu(args, rank, world, local_rank):
     e0.record(stream)
     up_stream.wait_event(e0)
     down_stream.wait_event(e0)
-    e2e_run(args.steps)
+    e2e_steps = max(args.steps, E2E_MIN_STEPS)
+    e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -691,8 +698,8 @@ def run_gpu(args, rank, world, local_rank):
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_sus"],
                      "peak_source": f"{pk['src']} bf16 sustained (kernel timed inside a long step)",
                      "traffic": traffic},
-        "e2e": {"value": world * tokens_per_step * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 12 * args.steps,
         "clocks": clocks,
         "backward": bwd,
