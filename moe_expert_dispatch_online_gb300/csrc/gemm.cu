@@ -817,25 +817,26 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 // gradient exactly as the single-CTA kernel does (same tiles of 32 x 32 fp32, same
 // K order, so the sums are the same bit for bit).
 //   barriers        owner   arrivals
-//   full[s]         CTA 0   CTA 0's producer (expect_tx) + CTA 0's TMA bytes + CTA 1's TMA bytes
-//                           (CTA 1's except in a tail stage)
-//   ptail[k % 8]    CTA 1   CTA 1's producer (expect_tx) + CTA 1's TMA bytes of the k-th tail stage
-//   zpeer[k % 8]    CTA 0   CTA 1's warp 1, once CTA 1's rows of the k-th tail stage are zero
+//   full[s]         CTA 0   CTA 0's producer (expect_tx) + both CTAs' TMA bytes; in a tail
+//                           stage only a plain arrive from CTA 0's producer
+//   ptail[k % 8]    both    own producer (expect_tx) + own TMA bytes of the k-th tail stage
+//   zpeer[k % 8]    CTA 0   each CTA's tail warp, once its rows of the k-th tail stage are zero
 //   empty[s]        both    the MMA thread's multicast commit
 //   tfull[a]        both    the MMA thread's multicast commit at the end of a unit
 //   tempty[a]       CTA 0   the 8 epilogue warps of each CTA
 // CTA 1's loads count on CTA 0's full barrier, so CTA 0 knows when the whole stage
 // is in. A segment's last K block usually holds rows of the next segment: in that
-// "tail stage" each CTA zeroes the extra rows of its own tiles. CTA 1 loads its tail
-// stage onto its own barrier, zeroes, and tells CTA 0 with one remote arrive per
-// unit, ahead of the MMAs that need it. The ring holds 6 stages, so at most 6 tail
+// "tail stage" each CTA loads its tiles onto its own barrier, and a tail warp of each
+// CTA zeroes the extra rows and tells CTA 0's MMA thread (CTA 1 with one remote
+// arrive per unit), ahead of the MMAs that need it and off the MMA thread. The ring holds 6 stages, so at most 6 tail
 // stages are loaded and not yet consumed; 8 ptail and 8 zpeer barriers therefore
 // never see two unobserved phases, which a parity wait could not tell apart.
 // Every wait is bounded; the CTAs meet at a cluster barrier before TMEM is freed
 // and either exits.
 constexpr int kPairStages = 6;
 constexpr int kPairEpiWarps = 8;
-constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
+constexpr int kPairTailWarp = 2 + kPairEpiWarps;   // warp that zeroes its CTA's tail rows
+constexpr int kPairThreads = 32 * (3 + kPairEpiWarps);
 constexpr int kPairHalf = 2 * kBChunkBytes;   // 16 KB: one CTA's A (or B) tile of a K block
 constexpr int kPairTails = 8;                 // ptail / zpeer barriers (> stages in the ring)
 constexpr int kPairBars = 2 * kPairStages + 4 + 2 * kPairTails;
@@ -877,7 +878,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
         }
         for (int k = 0; k < kPairTails; ++k) {
             mbar_init(&ptail[k], 1);
-            mbar_init(&zpeer[k], 1);
+            mbar_init(&zpeer[k], 2);
         }
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -928,19 +929,21 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                         live = false;
                         break;
                     }
-                    // CTA 0's barrier counts both CTAs' 32 KB, except that CTA 1's tail
-                    // stage counts on CTA 1's own barrier
+                    // CTA 0's barrier counts both CTAs' 32 KB, except in a tail stage, whose
+                    // bytes each CTA counts on its own ptail barrier (its tail warp zeroes
+                    // the extra rows); CTA 0 then completes the stage's full phase at once
                     const bool tstage = kb == kb_n - 1 && (tail & 15);
                     const int r0 = t.row0 + kb * kBK;
-                    if (!lead && tstage) {
+                    if (tstage) {
                         uint64_t* tb = &ptail[tk++ % kPairTails];
                         mbar_arrive_expect_tx(tb, 2 * kPairHalf);
                         for (int c = 0; c < 2; ++c) {
                             tma_load_2d(&tmA, tb, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
                             tma_load_2d(&tmB, tb, smB + s * kPairHalf + c * kBChunkBytes, n0 + c * 64, r0);
                         }
+                        if (lead) mbar_arrive(&full[s]);
                     } else {
-                        if (lead) mbar_arrive_expect_tx(&full[s], (tstage ? 2 : 4) * kPairHalf);
+                        if (lead) mbar_arrive_expect_tx(&full[s], 4 * kPairHalf);
                         const uint32_t bar = cluster_addr(&full[s], 0);
                         for (int c = 0; c < 2; ++c) {
                             tma_load_2d_pair(&tmA, bar, smA + s * kPairHalf + c * kBChunkBytes, h0 + c * 64, r0);
@@ -955,11 +958,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------- CTA 0: MMA issuer; CTA 1: tail rows
+        // ---------------------------------------------------- MMA issuer (CTA 0 only)
         // A segment's last K block usually holds rows of the next segment past
-        // `tail`: only its first ceil(tail/16) K steps are issued, and the rows of
-        // the last issued step past `tail` (at most 15) are zeroed in the A and B
-        // tiles of both CTAs before the MMAs read them, each CTA its own.
+        // `tail`: only its first ceil(tail/16) K steps are issued, after the tail
+        // warps of both CTAs have zeroed the rows of the last issued step past `tail`
+        // (at most 15) in their A and B tiles.
         if (lead) {
             const uint32_t idesc = idesc_bf16(kPairBM, kPairBN, true, true);
             uint32_t s = 0, ph = 0, zc = 0;
@@ -984,10 +987,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                         live = false;
                         break;
                     }
-                    if (tstage) {
-                        ++zc;
-                        zero_tail_rows(smA + s * kPairHalf, smB + s * kPairHalf, tail, lane);
-                    }
+                    if (tstage) ++zc;
                     const int ksteps = last ? (tail + 15) / 16 : kBK / 16;
                     if (lane == 0) {
                         tc_fence_after();
@@ -1008,9 +1008,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                 }
                 if (live && lane == 0) mma_commit_pair(&tfull[acc]);
             }
-        } else {
-            // CTA 1: follow the stage sequence; in each unit's tail stage wait for the
-            // own bytes, zero the tail rows and release the stage to CTA 0's MMA thread
+        }
+    } else if (warp == kPairTailWarp) {
+        // ---------------------------------------------------- tail rows (both CTAs)
+        // Follow the stage sequence; in each unit's tail stage wait for the CTA's own
+        // bytes, zero the rows past the segment end and release the stage to CTA 0's MMA
+        // thread (zpeer counts one arrival from each CTA).
+        {
             uint32_t s = 0, tc = 0;
             for (int unit = cl0; unit < total; unit += ncl) {
                 MTile t;
@@ -1023,7 +1027,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                                                        s_abort, status)))
                     break;
                 zero_tail_rows(smA + st * kPairHalf, smB + st * kPairHalf, tail, lane);
-                if (lane == 0) mbar_arrive_rank(&zpeer[tc % kPairTails], 0);
+                if (lane == 0) {
+                    if (lead) mbar_arrive(&zpeer[tc % kPairTails]);
+                    else mbar_arrive_rank(&zpeer[tc % kPairTails], 0);
+                }
                 ++tc;
                 __syncwarp();
             }
