@@ -33,7 +33,8 @@
 //     operand tiles in shared memory before lane 0 issues the MMAs that read them.
 // When 256 divides H and H', DW runs instead on clusters of two CTAs that share
 // each 256 x 256 gradient tile (grouped_gemm_dw_pair_kernel, cta_group::2): half
-// the operand bytes per SM and a six-stage ring.
+// the operand bytes per SM and a six-stage ring; there a separate tail warp in
+// each CTA zeroes its own tile's rows past a segment end.
 // Every mbarrier wait is bounded (2 s on the global timer); on expiry the CTA
 // records BEP_DERR_TIMEOUT, every role leaves its loop, and TMEM is freed.
 
