@@ -351,8 +351,8 @@ def run_gpu(args, rank, world, local_rank):
         drecv = torch.empty((R * S * K, H), dtype=torch.bfloat16, device=dev)
         dx = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
         nb = min(args.steps, 2 * len(topks))
-        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
-        nseg = []
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
+        nseg, nwrite = [], []
         for i in range(nb + 1):
             step(i)            # plan, dispatch, GEMM, combine, combine_bwd for routing i
             ev = bev[i - 1] if i > 0 else None
@@ -367,7 +367,13 @@ def run_gpu(args, rank, world, local_rank):
             bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red, stream)
             if ev is not None:
                 ev[3].record(stream)
+            # the same gradient written instead of added (a step's first micro-batch)
+            bep.bep_grouped_gemm_dw_overwrite(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red,
+                                              stream)
+            if ev is not None:
+                ev[4].record(stream)
                 nseg.append(int((buf.cu_seqlens[:, 1:] > buf.cu_seqlens[:, :-1]).sum().item()))
+                nwrite.append(E + int((buf.slot_expert >= 0).sum().item()))
         torch.cuda.synchronize()
         st = bep.bep_status(ctx, stream)
         if st:
@@ -375,8 +381,10 @@ def run_gpu(args, rank, world, local_rank):
         dx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bev)
         db_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in bev)
         dw_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
+        dwo_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in bev)
         flops = 2.0 * R * S * K * H * Hp
         dw_bytes = statistics.mean(nseg) * H * Hp * 4 * 2 + R * S * K * (H + Hp) * 2
+        dwo_bytes = statistics.mean(nwrite) * H * Hp * 4 + R * S * K * (H + Hp) * 2
         db_bytes = R * S * K * H * 2 + R * S * H * 2 + R * S * K * 4
         bwd = {
             "grouped_gemm_dx": {"ms": dx_ms, "tflops": flops / (dx_ms * 1e-3) / 1e12,
@@ -387,6 +395,11 @@ def run_gpu(args, rank, world, local_rank):
                                 "frac_bf16_sustained": flops / (dw_ms * 1e-3) / 1e12 / peaks()["bf16_sus"],
                                 "fp32_rmw_gbs": dw_bytes / (dw_ms * 1e-3) / 1e9,
                                 "segments": statistics.mean(nseg)},
+            "grouped_gemm_dw_overwrite": {
+                "ms": dwo_ms, "tflops": flops / (dwo_ms * 1e-3) / 1e12,
+                "frac_bf16_sustained": flops / (dwo_ms * 1e-3) / 1e12 / peaks()["bf16_sus"],
+                "fp32_write_gbs": dwo_bytes / (dwo_ms * 1e-3) / 1e9,
+                "rows_written": statistics.mean(nwrite)},
             "launches": nb,
         }
         del drecv, dx

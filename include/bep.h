@@ -243,6 +243,25 @@ int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
 int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
                         const uint16_t* dy, float* g_home, float* red, void* stream);
 
+/* The same weight gradient written instead of added (a GEMM with beta = 0), for
+ * the first micro-batch of a step, whose gradient buffers would otherwise have
+ * to be zeroed first:
+ *   g_home[e]          = recv[seg]^T @ dy[seg]  for every expert e, seg = its
+ *                        home segment (rank e / (E/R), row e); zeros when that
+ *                        segment is empty (all of e's tokens went to replicas,
+ *                        or none were routed to e)
+ *   red[u][rho - E]    = recv[seg]^T @ dy[seg]  for every non-empty slot segment;
+ *                        slots without tokens are not written
+ * bf16 in, fp32 accumulate, the fp32 sums stored as they are. reduce_grad then
+ * adds the replica slots into the home rows as after bep_grouped_gemm_dw.
+ * Arguments, layouts, restrictions and errors as bep_grouped_gemm_dw, and one
+ * more: the table must be a training plan's, with home row e used only on e's
+ * home rank; a non-empty row e < E on any other rank is refused on the device
+ * (BEP_DERR_BOUNDS latched, nothing written). With S*K == 0 only g_home is
+ * touched (zeroed); cu_seqlens, recv, dy and red may then be NULL. */
+int bep_grouped_gemm_dw_overwrite(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                                  const uint16_t* dy, float* g_home, float* red, void* stream);
+
 /* reduce_grad ([P2]; [P4] "The memory contract": each rank reads its own
  * experts' slots from every rank's reduce buffer, accumulates them into its
  * parameter gradient and zeroes the consumed slots):

@@ -38,6 +38,7 @@ BEP_INFER = 1
 SYMBOLS = ("bep_create", "bep_destroy", "bep_plan", "bep_plan_noalloc", "bep_prefetch_weight",
            "bep_dispatch", "bep_grouped_gemm", "bep_combine", "bep_combine_bwd",
            "bep_combine_dgates", "bep_dispatch_bwd", "bep_grouped_gemm_dx", "bep_grouped_gemm_dw",
+           "bep_grouped_gemm_dw_overwrite",
            "bep_grouped_gemm_vm", "bep_weights_create", "bep_weights_get",
            "bep_weights_destroy", "bep_reduce_grad", "bep_set_comm_sms", "bep_wait_selftest",
            "bep_status", "bep_clear_status", "bep_strerror")
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
             "bep_dispatch_bwd": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_grouped_gemm_dx": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_grouped_gemm_dw": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
+            "bep_grouped_gemm_dw_overwrite": (ctypes.c_int, [vp, p, p, p, p, p, vp]),
             "bep_reduce_grad": (ctypes.c_int, [vp, p, p, p, vp]),
             "bep_status": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "bep_clear_status": (ctypes.c_int, [vp, vp]),
@@ -419,17 +421,29 @@ def bep_grouped_gemm_dx(ctx: Context, cu_seqlens, dy, w_home, w_slots, drecv, st
            "bep_grouped_gemm_dx")
 
 
-def bep_grouped_gemm_dw(ctx: Context, cu_seqlens, recv, dy, g_home, red, stream=None):
+def _grouped_gemm_dw(name, ctx, cu_seqlens, recv, dy, g_home, red, stream):
     c = ctx.cfg
     _numel(cu_seqlens, c.R * (c.E + c.B + 1), "cu_seqlens")
     _numel(recv, c.R * c.C * c.H, "recv")
     _numel(dy, c.R * c.C * c.Hp, "dy")
     _numel(g_home, c.E * c.H * c.Hp, "g_home")
     _numel(red, c.R * c.B * c.H * c.Hp, "red")
-    _check(load().bep_grouped_gemm_dw(ctx.handle, _ptr(cu_seqlens, _i32(), "cu_seqlens"),
-                                      _ptr(recv, _bf16(), "recv"), _ptr(dy, _bf16(), "dy"),
-                                      _ptr(g_home, _f32(), "g_home"), _ptr(red, _f32(), "red"),
-                                      _stream(stream)), "bep_grouped_gemm_dw")
+    _check(getattr(load(), name)(ctx.handle, _ptr(cu_seqlens, _i32(), "cu_seqlens"),
+                                 _ptr(recv, _bf16(), "recv"), _ptr(dy, _bf16(), "dy"),
+                                 _ptr(g_home, _f32(), "g_home"), _ptr(red, _f32(), "red"),
+                                 _stream(stream)), name)
+
+
+def bep_grouped_gemm_dw(ctx: Context, cu_seqlens, recv, dy, g_home, red, stream=None):
+    """g_home[e] / red[u][j] += recv[seg]^T @ dy[seg] for every non-empty segment."""
+    _grouped_gemm_dw("bep_grouped_gemm_dw", ctx, cu_seqlens, recv, dy, g_home, red, stream)
+
+
+def bep_grouped_gemm_dw_overwrite(ctx: Context, cu_seqlens, recv, dy, g_home, red, stream=None):
+    """g_home[e] = its home segment's recv^T @ dy (zeros when empty) for every expert;
+    red[u][j] = recv[seg]^T @ dy[seg] for every non-empty slot segment."""
+    _grouped_gemm_dw("bep_grouped_gemm_dw_overwrite", ctx, cu_seqlens, recv, dy, g_home, red,
+                     stream)
 
 
 def bep_reduce_grad(ctx: Context, slot_expert, g_home, red, stream=None):

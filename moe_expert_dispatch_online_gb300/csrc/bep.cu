@@ -276,19 +276,36 @@ int bep_grouped_gemm_dx(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t*
                                                drecv, ctx->num_sms, as_stream(stream)));
 }
 
-int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
-                        const uint16_t* dy, float* g_home, float* red, void* stream) {
-    BEP_RANGE("bep_grouped_gemm_dw");
+static int grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                           const uint16_t* dy, float* g_home, float* red, int accumulate,
+                           void* stream) {
     if (!ctx) return BEP_ERR_ARG;
     if (ctx->d.mode != BEP_TRAIN) return BEP_ERR_MODE;
     if (ctx->d.H % bep::kBM != 0) return BEP_ERR_SIZE;
-    if (ctx->d.C == 0) return BEP_OK;
-    if (!cu_seqlens || !recv || !dy || !g_home || !red) return BEP_ERR_ARG;
-    if (!aligned(cu_seqlens, 4) || !aligned(recv, 16) || !aligned(dy, 16) ||
-        !aligned(g_home, 16) || !aligned(red, 16))
-        return BEP_ERR_ALIGN;
+    if (ctx->d.C == 0 && accumulate) return BEP_OK;
+    if (ctx->d.C == 0) {   // nothing to multiply: the overwrite zeroes the home rows
+        if (!g_home) return BEP_ERR_ARG;
+        if (!aligned(g_home, 16)) return BEP_ERR_ALIGN;
+    } else {
+        if (!cu_seqlens || !recv || !dy || !g_home || !red) return BEP_ERR_ARG;
+        if (!aligned(cu_seqlens, 4) || !aligned(recv, 16) || !aligned(dy, 16) ||
+            !aligned(g_home, 16) || !aligned(red, 16))
+            return BEP_ERR_ALIGN;
+    }
     return cuda_rc(bep::launch_grouped_gemm_dw(ctx->d, ctx->ws, cu_seqlens, recv, dy, g_home, red,
-                                               ctx->num_sms, as_stream(stream)));
+                                               accumulate, ctx->num_sms, as_stream(stream)));
+}
+
+int bep_grouped_gemm_dw(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                        const uint16_t* dy, float* g_home, float* red, void* stream) {
+    BEP_RANGE("bep_grouped_gemm_dw");
+    return grouped_gemm_dw(ctx, cu_seqlens, recv, dy, g_home, red, 1, stream);
+}
+
+int bep_grouped_gemm_dw_overwrite(bep_ctx* ctx, const int32_t* cu_seqlens, const uint16_t* recv,
+                                  const uint16_t* dy, float* g_home, float* red, void* stream) {
+    BEP_RANGE("bep_grouped_gemm_dw_overwrite");
+    return grouped_gemm_dw(ctx, cu_seqlens, recv, dy, g_home, red, 0, stream);
 }
 
 int bep_reduce_grad(bep_ctx* ctx, const int32_t* slot_expert, float* g_home, float* red,

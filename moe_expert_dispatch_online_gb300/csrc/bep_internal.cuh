@@ -97,7 +97,7 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
                                    cudaStream_t st);
 cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
                                    const uint16_t* recv, const uint16_t* dy, float* g_home,
-                                   float* red, int num_sms, cudaStream_t st);
+                                   float* red, int accumulate, int num_sms, cudaStream_t st);
 
 __device__ __forceinline__ int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }

@@ -389,6 +389,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   of them. Otherwise (training sizes: a few short segments among many long ones)
 //   the order is plain (rank, row, m).
 // seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
+// seg_mode == 2: as 1, plus an entry with rows = 0 for every expert whose home segment
+//   (rank e / (E/R), row e) is empty, so that an overwriting DW writes its zeros; a
+//   non-empty home row on any other rank refuses the table.
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
     __shared__ int s_warp[33];
@@ -405,6 +408,13 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         }
         *start = a;
         *len = b - a;
+        if (seg_mode == 2 && rho < d.E) {
+            // a training plan uses home row e only on e's home rank; another rank's rows
+            // there would make two units write one gradient row
+            if (u == rho / (d.E / d.R)) return 1;
+            if (b > a) bad = 1;
+            return 0;
+        }
         if (seg_mode) return b > a ? 1 : 0;
         return (b - a + kBM - 1) / kBM;
     };
@@ -480,6 +490,7 @@ struct GemmParams {
     int tmem_cols;
     int mtd;             // DW: m-blocks per weight row (H / 128)
     int vm;              // FWD / DX: weights as R consecutive [E+B, H, H'] views (tmB0)
+    int accumulate;      // DW: 1 = add the products to the gradient, 0 = write them
     int32_t* status;
 };
 
@@ -711,7 +722,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
                 for (int c0 = c_lo; c0 < c_lo + cspan; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                    if (u.t.rows > 0) {
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                    } else {   // an empty home segment (overwrite only): its gradient is zero
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
                     if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
                     __syncwarp();
 #pragma unroll
@@ -720,7 +736,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
-                        tma_reduce_add_2d(tmO, stg, u.nt * BN + c0, orow0);
+                        if (p.accumulate) tma_reduce_add_2d(tmO, stg, u.nt * BN + c0, orow0);
+                        else tma_store_2d(tmO, stg, u.nt * BN + c0, orow0);
                         bulk_commit();
                     }
                 }
@@ -1060,7 +1077,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
             uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
             for (int c0 = c_lo; c0 < c_lo + kPairBN / 2; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                if (t.rows > 0) {
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+                } else {   // an empty home segment (overwrite only): its gradient is zero
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
                 if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
                 __syncwarp();
 #pragma unroll
@@ -1069,7 +1091,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
-                    tma_reduce_add_2d(tmO, stg, nt * kPairBN + c0, orow0);
+                    if (p.accumulate) tma_reduce_add_2d(tmO, stg, nt * kPairBN + c0, orow0);
+                    else tma_store_2d(tmO, stg, nt * kPairBN + c0, orow0);
                     bulk_commit();
                 }
             }
@@ -1343,11 +1366,13 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
 
 cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int32_t* cu,
                                    const uint16_t* recv, const uint16_t* dy, float* g_home,
-                                   float* red, int num_sms, cudaStream_t st) {
-    if (d.C == 0) return cudaSuccess;
+                                   float* red, int accumulate, int num_sms, cudaStream_t st) {
+    if (d.C == 0)   // no rows: every home segment is empty
+        return accumulate ? cudaSuccess
+                          : cudaMemsetAsync(g_home, 0, (size_t)d.E * d.H * d.Hp * sizeof(float), st);
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 1);
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, accumulate ? 1 : 2);
     const int BN = pick_bn(d.Hp);
     CUtensorMap tmA, tmB;
     // A: recv^T in 64 (h) x 64 (row) boxes; B: dY in 64 (h') x 64 (row) boxes
@@ -1369,6 +1394,7 @@ cudaError_t launch_grouped_gemm_dw(const Dims& d, const Workspace& ws, const int
     prm.BN = BN;
     prm.tmem_cols = tmem_cols_for(BN);
     prm.mtd = d.H / kBM;
+    prm.accumulate = accumulate;
     prm.status = ws.status;
     // SM pairs when the tile divides the gradient: 256 x 256 tiles, six-stage rings
     int dev = 0;

@@ -9,8 +9,9 @@ pairs or on single CTAs), inference with and without overflow rows.
 Checked through the C ABI:
   plan (cu_seqlens, slot map, dest, maxvio), prefetch, dispatch, combine
   backward, dispatch backward and reduce_grad bit for bit;
-  forward and dX GEMMs per segment, dW per weight row (training), and the
-  combined output, each within 2e-2 relative of binary64.
+  forward and dX GEMMs per segment, dW per weight row (training; both the
+  accumulating and the overwriting form), and the combined output, each within
+  2e-2 relative of binary64.
 """
 import numpy as np
 import pytest
@@ -150,6 +151,8 @@ def run_chain(bep, c, topk, seed):
         red = torch.zeros((R, B, H, Hp), dtype=torch.float32, device=DEV)
         with pytest.raises(bep.BepError):
             bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, buf.dy, g, red)
+        with pytest.raises(bep.BepError):
+            bep.bep_grouped_gemm_dw_overwrite(ctx, buf.cu_seqlens, buf.recv, buf.dy, g, red)
     elif mode == 0:
         # dW into the gradients, then reduce_grad folds the replica rows into the home rows
         g0 = synth.normal_host((E, H, Hp), 50 + seed, 0.5)
@@ -173,6 +176,28 @@ def run_chain(bep, c, topk, seed):
                     assert err <= RTOL, (c, u, j, err)
                 else:
                     np.testing.assert_array_equal(rh[u, j], red0[u, j])
+        # the overwriting form on poisoned buffers: home rows written (zeros where the home
+        # segment is empty), used slots written, the other slots untouched
+        gw = torch.full((E, H, Hp), 7.0, dtype=torch.float32, device=DEV)
+        rw = torch.full((R, B, H, Hp), 7.0, dtype=torch.float32, device=DEV)
+        bep.bep_grouped_gemm_dw_overwrite(ctx, buf.cu_seqlens, buf.recv, buf.dy, gw, rw)
+        torch.cuda.synchronize()
+        assert bep.bep_status(ctx) == 0, c
+        gwh, rwh = gw.cpu().numpy(), rw.cpu().numpy()
+        for e in range(E):
+            if d_home[e].any():
+                err = np.linalg.norm(gwh[e] - d_home[e]) / np.linalg.norm(d_home[e])
+                assert err <= RTOL, (c, e, err)
+            else:
+                assert (gwh[e] == 0).all(), (c, e)
+        for u in range(R):
+            for j in range(B):
+                if ref.slot_expert[u, j] >= 0:
+                    err = np.linalg.norm(rwh[u, j] - d_slots[u, j]) / np.linalg.norm(d_slots[u, j])
+                    assert err <= RTOL, (c, u, j, err)
+                else:
+                    assert (rwh[u, j] == 7.0).all(), (c, u, j)
+        del gw, rw
         g_ref, red_ref = gh.copy(), rh.copy()
         oracle.reduce_grad(g_ref, red_ref, ref.slot_expert)
         bep.bep_reduce_grad(ctx, buf.slot_expert, g, red)
