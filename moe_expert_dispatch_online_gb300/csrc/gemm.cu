@@ -23,8 +23,9 @@
 //   * warp 0 issues TMA loads (128-byte swizzle) into a 4-stage shared-memory
 //     ring guarded by mbarriers;
 //   * warp 1 (lane 0) issues tcgen05.mma.kind::f16 (M=128, N=BN<=256, K=16,
-//     bf16 in, fp32 accumulate) into one of two TMEM accumulators; tcgen05.commit
-//     frees each stage and publishes each finished tile;
+//     bf16 in, fp32 accumulate; M=64 for a FWD/DX m-tile of at most 64 rows) into
+//     one of two TMEM accumulators; tcgen05.commit frees each stage and publishes
+//     each finished tile;
 //   * 4 (DW: 8) epilogue warps drain the other accumulator with tcgen05.ld:
 //     FWD/DX round to bf16 (nearest even) and store only the rows inside the
 //     segment; DW adds the fp32 tile into the gradient rows;
@@ -635,12 +636,16 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         // the rows of the last issued step past `tail` (at most 15) are zeroed in
         // both operand tiles by all 32 lanes (whole 128-byte rows, so the
         // swizzle does not matter) before lane 0 issues the MMAs.
-        const uint32_t idesc = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
+        // FWD/DX: an m-tile of at most 64 rows (a segment's last) runs M=64 MMAs, which
+        // put row r of the accumulator in TMEM lane 32 * (r / 16) + r % 16
+        const uint32_t idesc_full = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
+        const uint32_t idesc_half = idesc_bf16(kBM / 2, BN, CF::kAmn, CF::kBmn);
         uint32_t s = 0, ph = 0;
         bool live = true;
         int it = 0;
         for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
             const Unit u = unit_at<MODE>(p, unit, NT);
+            const uint32_t idesc = (MODE != kDw && u.t.rows <= kBM / 2) ? idesc_half : idesc_full;
             const int acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
@@ -750,9 +755,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 // four whole 128-byte lines), skipping the rows past the segment end, which
                 // belong to the next segment's tile. Two boxes per warp alternate, so one
                 // store can be in flight while the next box is filled.
-                const int nvalid = u.t.rows - q * 32;   // this warp's rows inside the segment
+                // this warp's rows: 32q..32q+31 of a full tile, or, of an M=64 tile,
+                // 16q..16q+15 in lanes 0-15 of its quadrant
+                const int wrows = u.t.rows <= kBM / 2 ? 16 : 32;
+                const int nvalid = min(wrows, u.t.rows - q * wrows);   // of them inside the segment
                 const int rsub = lane >> 3, piece = lane & 7;
-                const int orow = u.t.row0 + q * 32;
+                const int orow = u.t.row0 + q * wrows;
                 uint16_t* ybase = p.out + (int64_t)orow * p.N + (int64_t)u.nt * BN;
                 for (int c0 = c_lo; c0 < c_lo + cspan && nvalid > 0; c0 += 64) {
                     const int b = obox++ & 1;
@@ -780,7 +788,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                             srow[(4 * h + v) ^ (lane & 7)] = o;
                         }
                     }
-                    if (nvalid >= 32) {
+                    if (nvalid == 32) {
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                         if (lane == 0) {
