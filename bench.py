@@ -351,11 +351,13 @@ def run_gpu(args, rank, world, local_rank):
         drecv = torch.empty((R * S * K, H), dtype=torch.bfloat16, device=dev)
         dx = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
         nb = min(args.steps, 2 * len(topks))
-        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(nb)]
         nseg, nwrite = [], []
         for i in range(nb + 1):
-            step(i)            # plan, dispatch, GEMM, combine, combine_bwd for routing i
             ev = bev[i - 1] if i > 0 else None
+            if ev is not None:
+                ev[5].record(stream)
+            step(i)            # plan, dispatch, GEMM, combine, combine_bwd for routing i
             if ev is not None:
                 ev[0].record(stream)
             bep.bep_grouped_gemm_dx(ctx, buf.cu_seqlens, buf.dy, w_home, w_slots, drecv, stream)
@@ -364,12 +366,12 @@ def run_gpu(args, rank, world, local_rank):
             bep.bep_dispatch_bwd(ctx, drecv, buf.dest, dx, stream)
             if ev is not None:
                 ev[2].record(stream)
-            bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red, stream)
-            if ev is not None:
-                ev[3].record(stream)
-            # the same gradient written instead of added (a step's first micro-batch)
+            # the weight gradient written (a step's first micro-batch), then added (a later one)
             bep.bep_grouped_gemm_dw_overwrite(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red,
                                               stream)
+            if ev is not None:
+                ev[3].record(stream)
+            bep.bep_grouped_gemm_dw(ctx, buf.cu_seqlens, buf.recv, buf.dy, g_home, red, stream)
             if ev is not None:
                 ev[4].record(stream)
                 nseg.append(int((buf.cu_seqlens[:, 1:] > buf.cu_seqlens[:, :-1]).sum().item()))
@@ -380,8 +382,10 @@ def run_gpu(args, rank, world, local_rank):
             raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
         dx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bev)
         db_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in bev)
-        dw_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
-        dwo_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in bev)
+        dwo_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
+        dw_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in bev)
+        # one layer's forward and backward: the step's rows, dX, dispatch backward, dW
+        layer_ms = statistics.mean(e[5].elapsed_time(e[3]) for e in bev)
         flops = 2.0 * R * S * K * H * Hp
         dw_bytes = statistics.mean(nseg) * H * Hp * 4 * 2 + R * S * K * (H + Hp) * 2
         dwo_bytes = statistics.mean(nwrite) * H * Hp * 4 + R * S * K * (H + Hp) * 2
@@ -400,6 +404,9 @@ def run_gpu(args, rank, world, local_rank):
                 "frac_bf16_sustained": flops / (dwo_ms * 1e-3) / 1e12 / peaks()["bf16_sus"],
                 "fp32_write_gbs": dwo_bytes / (dwo_ms * 1e-3) / 1e9,
                 "rows_written": statistics.mean(nwrite)},
+            "layer_fwd_bwd": {"ms": layer_ms, "tokens_per_s": R * S / (layer_ms * 1e-3),
+                              "kernels": "plan, prefetch, dispatch, GEMM, combine, combine_bwd, "
+                                         "reduce_grad, dX GEMM, dispatch_bwd, dW GEMM (overwriting)"},
             "launches": nb,
         }
         del drecv, dx
