@@ -281,40 +281,58 @@ __global__ void __launch_bounds__(kThreads) combine_dgates_kernel(const uint4* _
 
 // ----------------------------------------------------------------------------- prefetch
 // w_slots[s] = w_home[slot_expert[s]] for every used slot s = u*B + j. Each slot is
-// one contiguous [H, H'] block; CTAs stride over 32 KB tiles of it, slot after slot.
+// one contiguous [H, H'] block of 32 KB tiles; the (used slot, tile) pairs are spread
+// over the whole grid, slot by slot, so every CTA copies about the same number of tiles.
 constexpr int kCopyU = 8;   // 16-byte vectors per thread per tile
 
 __global__ void __launch_bounds__(kThreads) prefetch_kernel(const int32_t* __restrict__ slot_expert,
                                                             const uint4* __restrict__ w_home,
                                                             uint4* __restrict__ w_slots, int nslots,
                                                             int E, int64_t nvec, int32_t* status) {
-    __shared__ int32_t s_se[kMaxE];   // nslots = R*B <= E <= kMaxE
-    for (int s = threadIdx.x; s < nslots; s += blockDim.x) s_se[s] = slot_expert[s];
+    __shared__ int32_t s_slot[kMaxE];   // used slots in ascending order (nslots = R*B <= E <= kMaxE)
+    __shared__ int32_t s_exp[kMaxE];    // their experts
+    __shared__ int s_nused;
+    if (threadIdx.x < 32) {
+        // warp 0 lists the used slots: one ballot per 32 entries keeps their order
+        const int lane = threadIdx.x;
+        int n = 0;
+        for (int b = 0; b < nslots; b += 32) {
+            const int sl = b + lane;
+            int e = sl < nslots ? slot_expert[sl] : -1;
+            if (e >= E) {
+                if (blockIdx.x == 0) set_status(status, BEP_DERR_BOUNDS);
+                e = -1;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, e >= 0);
+            if (e >= 0) {
+                const int at = n + __popc(m & ((1u << lane) - 1u));
+                s_slot[at] = sl;
+                s_exp[at] = e;
+            }
+            n += __popc(m);
+        }
+        if (lane == 0) s_nused = n;
+    }
     __syncthreads();
     const int64_t tile_vec = (int64_t)kThreads * kCopyU;
     const int64_t ntile = (nvec + tile_vec - 1) / tile_vec;
-    for (int s = 0; s < nslots; ++s) {
-        const int e = s_se[s];
-        if (e < 0) continue;
-        if (e >= E) {
-            if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, BEP_DERR_BOUNDS);
-            continue;
+    const int64_t nwork = (int64_t)s_nused * ntile;
+    for (int64_t w = blockIdx.x; w < nwork; w += gridDim.x) {
+        const int k = (int)(w / ntile);
+        const int64_t t = w - (int64_t)k * ntile;
+        const uint4* src = w_home + (int64_t)s_exp[k] * nvec;
+        uint4* dst = w_slots + (int64_t)s_slot[k] * nvec;
+        const int64_t base = t * tile_vec + threadIdx.x;
+        uint4 v[kCopyU];
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) v[u] = ld_stream(src + i);
         }
-        const uint4* src = w_home + (int64_t)e * nvec;
-        uint4* dst = w_slots + (int64_t)s * nvec;
-        for (int64_t t = blockIdx.x; t < ntile; t += gridDim.x) {
-            const int64_t base = t * tile_vec + threadIdx.x;
-            uint4 v[kCopyU];
 #pragma unroll
-            for (int u = 0; u < kCopyU; ++u) {
-                const int64_t i = base + (int64_t)u * kThreads;
-                if (i < nvec) v[u] = ld_stream(src + i);
-            }
-#pragma unroll
-            for (int u = 0; u < kCopyU; ++u) {
-                const int64_t i = base + (int64_t)u * kThreads;
-                if (i < nvec) dst[i] = v[u];
-            }
+        for (int u = 0; u < kCopyU; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) dst[i] = v[u];
         }
     }
 }
