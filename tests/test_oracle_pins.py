@@ -655,3 +655,44 @@ def test_grouped_gemm_dw_one_hot_rows_are_outer_products():
         tgt[hot[i]] += dyv[i]
     np.testing.assert_array_equal(d_home, ref_home)
     np.testing.assert_array_equal(d_slots, ref_slots)
+
+
+def test_sampled_gemm_helpers_agree_with_the_whole_gemm():
+    """The helpers the bench-size parity tests use to check sampled rows --
+    segment_of_rows, weight_row_of and gemm_rows (and grouped_gemm's rows= form) --
+    give, row for row, what the whole grouped GEMM (pinned above by shift matrices
+    and brute force) gives, on an inference batch whose hot group overflows, so
+    home, slot and overflow segments all occur. segment_of_rows is also checked
+    against a plain search of cu_seqlens."""
+    R, E, B, K, S, H, Hp = 2, 16, 2, 2, 64, 64, 48
+    G = E // R
+    pop = np.full(E, 1.0)
+    pop[:G] = 200.0                                       # group 0's experts all hot
+    topk = synth.gumbel_topk(R, S, K, pop / pop.sum(), 11)
+    ref = oracle.plan(topk, E, B, 1)
+    assert oracle.check_plan(topk, E, B, 1, ref.cu, ref.slot_expert, ref.dest) == 0
+    C = S * K
+    x = synth.tokens_host((R, S, H), 12)
+    recv = oracle.dispatch(x, ref.dest)
+    w_home = synth.weights_host((E, H, Hp), 13)
+    w_slots = oracle.prefetch(w_home, ref.slot_expert, np.zeros((R, B, H, Hp), np.uint16))
+    y = oracle.grouped_gemm(recv, w_home, w_slots, ref.cu, E)
+    rows, segs = [], []
+    overflow = slot = 0
+    for u in range(R):
+        for rho in range(E + B):
+            a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+            if b > a:
+                rows += range(u * C + a, u * C + b)
+                segs += [rho] * (b - a)
+                overflow += int(rho < E and rho // G != u)
+                slot += int(rho >= E)
+    assert overflow > 0 and slot > 0                      # every kind of segment is present
+    rows = np.array(rows)
+    np.testing.assert_array_equal(oracle.segment_of_rows(ref.cu, C, rows), segs)
+    np.testing.assert_allclose(oracle.grouped_gemm(recv, w_home, w_slots, ref.cu, E, rows=rows),
+                               y[rows], rtol=1e-12, atol=1e-12)
+    for i, rho in zip(rows, segs):
+        e = oracle.weight_row_of(rho, i // C, E, ref.slot_expert)
+        np.testing.assert_allclose(oracle.gemm_rows(recv[i:i + 1], w_home[e])[0], y[i],
+                                   rtol=1e-12, atol=1e-12)
