@@ -419,19 +419,70 @@ def test_combine_bwd_matches_torch():
 
 
 # ---------------------------------------------------------------- prefetch / reduce_grad
-def test_prefetch_copies_home_rows():
-    topk, p, x, g, y = _small_problem(E=16, R=2)
-    E, B = 16, 8
-    w_home = synth.weights_host((E, 8, 16), 1)
-    w_slots = np.zeros((2, B, 8, 16), np.uint16)
+def _expert_pattern(e, H, Hp):
+    """A weight row that spells out its own expert id: element (h, h') is the
+    integer (e*131 + h*7 + h'*3) mod 251, exact in bf16 (every integer below 256 is)."""
+    h = np.arange(H)[:, None]
+    hp = np.arange(Hp)[None, :]
+    return _torch_bf16_bits(((e * 131 + h * 7 + hp * 3) % 251).astype(np.float32))
+
+
+@pytest.mark.parametrize("seed,R,E,S,K", [(0, 2, 16, 37, 4), (1, 4, 16, 60, 3), (2, 8, 32, 50, 4)])
+def test_prefetch_slots_hold_their_parents_experts(seed, R, E, S, K):
+    """Training mode ([P4] "The memory contract"): B = E/R and a replica of expert e
+    on rank u sits in slot j = e - parent(u)*G, so slot j of a rank that takes
+    replicas must hold expert parent(u)*G + j. Every home row is filled with a
+    pattern that encodes its expert id; the expected slot contents are that
+    pattern evaluated at the expert the training rule names -- not an index into
+    w_home -- and every slot the plan leaves unused keeps its sentinel bits."""
+    G, B, H, Hp = E // R, E // R, 6, 10
+    topk = synth.gumbel_topk(R, S, K, synth.zipf_popularity(E, 1.6), seed)
+    p = oracle.plan(topk, E, B, oracle.MODE_TRAIN)
+    assert (p.slot_expert >= 0).any()
+    w_home = np.stack([_expert_pattern(e, H, Hp) for e in range(E)])
+    sentinel = np.uint16(0x7FC1)      # a NaN pattern no pattern element can take
+    w_slots = np.full((R, B, H, Hp), sentinel, np.uint16)
     oracle.prefetch(w_home, p.slot_expert, w_slots)
-    for u in range(2):
+    for u in range(R):
+        # the slots a rank's segment rows E..E+B-1 actually use (cu_seqlens)
+        used_rows = [j for j in range(B) if p.cu[u, E + j + 1] > p.cu[u, E + j]]
+        assert used_rows == [j for j in range(B) if p.slot_expert[u, j] >= 0]
         for j in range(B):
-            e = p.slot_expert[u, j]
-            if e >= 0:
-                np.testing.assert_array_equal(w_slots[u, j], w_home[e])
+            if j in used_rows:
+                assert p.parent[u] >= 0
+                np.testing.assert_array_equal(w_slots[u, j],
+                                              _expert_pattern(p.parent[u] * G + j, H, Hp))
             else:
-                assert not w_slots[u, j].any()
+                assert (w_slots[u, j] == sentinel).all()
+
+
+def test_prefetch_inference_slots_hold_the_top_counted_remote_experts():
+    """Inference mode (B < E/R): a rank's slots hold, in ascending id, the B remote
+    experts with the most of its token-slots ([P4] "The memory contract", with the
+    overflow reading), and each such slot's contents are that expert's pattern."""
+    R, S, K, E, B, H, Hp = 4, 80, 4, 32, 2, 4, 8
+    G = E // R
+    pop = np.full(E, 1e-6)
+    pop[:G] = np.linspace(1.0, 2.0, G)
+    topk = synth.gumbel_topk(R, S, K, pop / pop.sum(), 3)
+    p = oracle.plan(topk, E, B, oracle.MODE_INFER)
+    w_home = np.stack([_expert_pattern(e, H, Hp) for e in range(E)])
+    w_slots = np.zeros((R, B, H, Hp), np.uint16)
+    oracle.prefetch(w_home, p.slot_expert, w_slots)
+    C = S * K
+    moved = 0
+    for u in range(R):
+        # count, from dest and topk alone, the token-slots of each remote expert on rank u
+        on_u = (p.dest // C) == u
+        cnt = np.bincount(topk[on_u].ravel(), minlength=E)
+        remote = [e for e in range(E) if cnt[e] > 0 and e // G != u]
+        top = sorted(sorted(remote, key=lambda e: (-cnt[e], e))[:B])
+        moved += len(top)
+        for j, e in enumerate(top):
+            np.testing.assert_array_equal(w_slots[u, j], _expert_pattern(e, H, Hp))
+        for j in range(len(top), B):
+            assert not w_slots[u, j].any()
+    assert moved > 0
 
 
 def test_reduce_grad_integer_values_exact_and_zeroed():
@@ -563,17 +614,44 @@ def test_dispatch_bwd_exact_on_dyadic_values():
     np.testing.assert_array_equal(dx, _torch_bf16_bits(exact.astype(np.float32)))
 
 
-def test_combine_dgates_brute_force():
+def test_combine_dgates_one_hot_dout_reads_one_element():
+    """dg[t,k] = <dOut[t], Y[dest[t,k]]> ([P4] "The core idea": the gradient of the
+    gate weight). With dOut[t] one-hot at column c_t the dot product is the single
+    element Y[dest[t,k], c_t], exactly."""
     topk, p, x, g, y = _small_problem(K=3, D=8, S=5)
     R, S, K = topk.shape
-    dout = synth.tokens_host((R, S, 8), 4)
+    D = y.shape[1]
+    c = np.random.default_rng(11).integers(0, D, size=(R, S))
+    dout = np.zeros((R, S, D), np.uint16)
+    dout[np.arange(R)[:, None], np.arange(S)[None, :], c] = 0x3F80      # bf16 1.0
     dg = oracle.combine_dgates(dout, y, p.dest)
-    yf, df = oracle.bf16_to_f32(y), oracle.bf16_to_f32(dout)
+    yf = oracle.bf16_to_f32(y)
     for r in range(R):
         for t in range(S):
             for k in range(K):
-                ref = sum(float(df[r, t, c]) * float(yf[p.dest[r, t, k], c]) for c in range(8))
-                assert abs(dg[r, t, k] - ref) <= 1e-12 * (1 + abs(ref))
+                assert dg[r, t, k] == float(yf[p.dest[r, t, k], c[r, t]])
+
+
+def test_combine_dgates_is_the_adjoint_of_combine():
+    """Combine is linear in the gates: out[t] = sum_k g[t,k] Y[dest[t,k]]. So
+    sum_{t,k} g[t,k] * dg[t,k] = <dOut, out> for any gates. The right side is
+    formed here as one fp64 tensor contraction of the gathered rows, with small
+    dyadic values so that both sides are exact sums."""
+    topk, p, x, _, _ = _small_problem(K=4, D=12, S=9, R=2)
+    R, S, K = topk.shape
+    rng = np.random.default_rng(12)
+    yv = rng.integers(-16, 17, size=(R * S * K, 12)).astype(np.float32) / 4
+    dv = rng.integers(-16, 17, size=(R, S, 12)).astype(np.float32) / 8
+    gv = rng.integers(-8, 9, size=(R, S, K)).astype(np.float64)
+    dg = oracle.combine_dgates(_torch_bf16_bits(dv), _torch_bf16_bits(yv), p.dest)
+    out = np.einsum("rsk,rskd->rsd", gv, yv[p.dest].astype(np.float64))
+    assert (gv * dg).sum() == (dv.astype(np.float64) * out).sum()
+    # and gate by gate: a one-hot gate vector isolates one dg entry
+    for r, t, k in [(0, 0, 0), (1, 8, 3), (0, 4, 2)]:
+        e = np.zeros_like(gv)
+        e[r, t, k] = 1.0
+        out = np.einsum("rsk,rskd->rsd", e, yv[p.dest].astype(np.float64))
+        assert dg[r, t, k] == (dv.astype(np.float64) * out).sum()
 
 
 def _shift_weights(E, R, B, H, Hp):
