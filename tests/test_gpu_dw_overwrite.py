@@ -9,11 +9,13 @@ on hand-made training tables (home rows only on their home rank, ragged lengths,
 empty home segments, +inf in every receive row outside the segments) on single
 CTAs (H'=128) and on SM pairs (H=512, H'=256); the sums equal, value for value,
 those the accumulating call adds onto zeros; a table that is not a training
-plan's is refused; S*K = 0 zeroes the home rows."""
+plan's is refused; S*K = 0 zeroes the home rows. Written rows are also checked
+element by element against the fp32-accumulation bound of ``elementwise``."""
 import numpy as np
 import pytest
 import torch
 
+import elementwise as ew
 import oracle
 import synth
 
@@ -87,6 +89,9 @@ def test_overwrite_matches_oracle_on_training_table(lib, H, HP):
                 continue
             err = np.linalg.norm(rh[u, j] - d_slots[u, j]) / np.linalg.norm(d_slots[u, j])
             assert err <= RTOL, (u, j, err)
+    worst = ew.dw_table(gh, rh, d_home, d_slots, oracle.bf16_to_f32(recv).astype(np.float64),
+                        oracle.bf16_to_f32(dy).astype(np.float64), cu, E, C)
+    print(f"overwriting dW (H={H}): {worst}")
 
 
 @pytest.mark.parametrize("H, HP", [(256, 128), (512, 256)])

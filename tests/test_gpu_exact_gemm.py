@@ -168,13 +168,14 @@ def test_weight_gradient_one_hot_rows_exact(lib):
     np.testing.assert_array_equal(red.cpu().numpy(), (red0 + d_slots).astype(np.float32))
 
 
-def test_forward_and_weight_gradient_exact_at_bench_size_sampled(lib):
+@pytest.mark.parametrize("target", [0.2, 1.0, 10.0, 20.0])
+def test_forward_and_weight_gradient_exact_at_bench_size_sampled(lib, target):
     """S=8192, E=384: forward with permutation weights on sampled rows of every rank's
     first, last and remote segments; weight gradient with one-hot rows on sampled
     rows of sampled home experts and slots."""
     bep = lib
     torch.cuda.empty_cache()
-    wl, ref, ctx, buf = planned(bep, "bench_r8_e384", 10.0)
+    wl, ref, ctx, buf = planned(bep, "bench_r8_e384", target)
     R, C, E, B, H, Hp = wl.R, wl.C, wl.E, wl.B, wl.H, wl.Hp
     n = R * C
     rng = np.random.default_rng(507)
@@ -244,14 +245,15 @@ def test_forward_and_weight_gradient_exact_at_bench_size_sampled(lib):
     torch.cuda.empty_cache()
 
 
-def test_overflow_rows_exact_at_inference_size_sampled(lib):
-    """S=512, B=4 < E/R, hot experts on group 0 (maxvio 20): segments of remote experts
-    beyond the B slots are overflow rows that read the home weights in place. Forward
-    and input gradient with permutation weights, exact on sampled rows of every rank's
-    overflow, slot and first home segments."""
+@pytest.mark.parametrize("target", [1.0, 20.0])
+def test_overflow_rows_exact_at_inference_size_sampled(lib, target):
+    """S=512, B=4 < E/R, hot experts on group 0 (maxvio 1 and 20): segments of remote
+    experts beyond the B slots are overflow rows that read the home weights in place.
+    Forward and input gradient with permutation weights, exact on sampled rows of
+    every rank's overflow, slot and first home segments."""
     bep = lib
     torch.cuda.empty_cache()
-    wl, ref, ctx, buf = planned(bep, "infer_r8_e384_b4", 20.0)
+    wl, ref, ctx, buf = planned(bep, "infer_r8_e384_b4", target)
     R, C, E, B, H, Hp, G = wl.R, wl.C, wl.E, wl.B, wl.H, wl.Hp, wl.E // wl.R
     rng = np.random.default_rng(511)
     x = synth.tokens_device((R, wl.S, H), 512)

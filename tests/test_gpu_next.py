@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import elementwise as ew
 import oracle
 import synth
 
@@ -125,3 +126,12 @@ def test_second_projection_shares_the_plan(lib):
     assert bep.bep_status(ctx) == 0 and bep.bep_status(ctx2) == 0
     got = oracle.bf16_to_f32(host_u16(out)).astype(np.float64)
     assert np.linalg.norm(got - out_ref) / np.linalg.norm(out_ref) <= RTOL
+    # the down projection alone, element by element, on the library's own first output
+    y1_gpu = host_u16(buf.y)
+    y2_ref = oracle.grouped_gemm(y1_gpu, w_dn, dn_slots, ref.cu, E)
+    wd = oracle.bf16_to_f32(w_dn).astype(np.float64)
+    wds = oracle.bf16_to_f32(dn_slots).astype(np.float64)
+    worst = ew.gemm_table("fwd", oracle.bf16_to_f32(host_u16(y2d)).astype(np.float64), y2_ref,
+                          oracle.bf16_to_f32(y1_gpu).astype(np.float64), ref.cu, E, S * K,
+                          lambda u, rho: wd[rho] if rho < E else wds[u, rho - E])
+    print(f"down projection: {worst}")

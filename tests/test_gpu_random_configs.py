@@ -11,12 +11,14 @@ Checked through the C ABI:
   backward, dispatch backward and reduce_grad bit for bit;
   forward and dX GEMMs per segment, dW per weight row (training; both the
   accumulating and the overwriting form), and the combined output, each within
-  2e-2 relative of binary64.
+  2e-2 relative of binary64; the three GEMMs also element by element against
+  the fp32-accumulation bound of ``elementwise``.
 """
 import numpy as np
 import pytest
 import torch
 
+import elementwise as ew
 import oracle
 import synth
 
@@ -124,6 +126,11 @@ def run_chain(bep, c, topk, seed):
             for u in range(R) for rho in range(E + B) if ref.cu[u, rho + 1] > ref.cu[u, rho]]
     for u, rho, a, b in segs:
         assert rel(y[u * C + a:u * C + b], y_ref[u * C + a:u * C + b]) <= RTOL, (c, u, rho)
+    wh = oracle.bf16_to_f32(w_home).astype(np.float64)
+    ws = oracle.bf16_to_f32(slots_ref).astype(np.float64)
+    weight = lambda u, rho: wh[rho] if rho < E else ws[u, rho - E]      # noqa: E731
+    recv_f = oracle.bf16_to_f32(recv_ref).astype(np.float64)
+    ew.gemm_table("fwd", y, y_ref, recv_f, ref.cu, E, C, weight)
     out_ref = oracle.bf16_to_f32(oracle.combine(oracle.f32_to_bf16(y_ref), ref.dest, gates))
     assert rel(oracle.bf16_to_f32(host_u16(buf.out)).astype(np.float64), out_ref) <= RTOL, c
     # the combine itself, bit for bit, on the GPU's own Y
@@ -143,6 +150,8 @@ def run_chain(bep, c, topk, seed):
     dr = oracle.bf16_to_f32(host_u16(drecv)).astype(np.float64)
     for u, rho, a, b in segs:
         assert rel(dr[u * C + a:u * C + b], dr_ref[u * C + a:u * C + b]) <= RTOL, (c, u, rho)
+    dy_f = oracle.bf16_to_f32(dy_ref).astype(np.float64)
+    ew.gemm_table("dx", dr, dr_ref, dy_f, ref.cu, E, C, weight)
     np.testing.assert_array_equal(host_u16(dx), oracle.dispatch_bwd(host_u16(drecv), ref.dest))
 
     if mode == 0 and H % 128 != 0:
@@ -176,6 +185,7 @@ def run_chain(bep, c, topk, seed):
                     assert err <= RTOL, (c, u, j, err)
                 else:
                     np.testing.assert_array_equal(rh[u, j], red0[u, j])
+        ew.dw_table(gh, rh, d_home, d_slots, recv_f, dy_f, ref.cu, E, C, g0, red0)
         # the overwriting form on poisoned buffers: home rows written (zeros where the home
         # segment is empty), used slots written, the other slots untouched
         gw = torch.full((E, H, Hp), 7.0, dtype=torch.float32, device=DEV)
@@ -197,6 +207,7 @@ def run_chain(bep, c, topk, seed):
                     assert err <= RTOL, (c, u, j, err)
                 else:
                     assert (rwh[u, j] == 7.0).all(), (c, u, j)
+        ew.dw_table(gwh, rwh, d_home, d_slots, recv_f, dy_f, ref.cu, E, C)
         del gw, rw
         g_ref, red_ref = gh.copy(), rh.copy()
         oracle.reduce_grad(g_ref, red_ref, ref.slot_expert)

@@ -4,11 +4,14 @@ K step and 64-row K block of the weight-gradient GEMM (its last block issues
 only the steps it holds and zeroes the rest of the last step), and the 128-row
 M tile of the forward and input-gradient GEMMs (rows past a segment end belong
 to the next segment and must not be written). Compared per segment / weight
-row with the binary64 oracle; rows outside every segment keep their contents."""
+row with the binary64 oracle (relative Frobenius, and every element against the
+fp32-accumulation bound of ``elementwise``); rows outside every segment keep
+their contents."""
 import numpy as np
 import pytest
 import torch
 
+import elementwise as ew
 import oracle
 import synth
 
@@ -84,6 +87,10 @@ def test_forward_on_ragged_segments(lib):
             err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
             assert err <= RTOL, (u, rho, b - a, err)
     assert (got[~covered(cu)] == -7.0).all()
+    wh, ws = oracle.bf16_to_f32(w_home).astype(np.float64), oracle.bf16_to_f32(w_slots).astype(np.float64)
+    worst = ew.gemm_table("fwd", got, ref, oracle.bf16_to_f32(recv).astype(np.float64), cu, E, C,
+                          lambda u, rho: wh[rho] if rho < E else ws[u, rho - E])
+    print(f"forward on ragged segments: {worst}")
 
 
 def test_input_gradient_on_ragged_segments(lib):
@@ -108,6 +115,10 @@ def test_input_gradient_on_ragged_segments(lib):
             err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
             assert err <= RTOL, (u, rho, b - a, err)
     assert (got[~covered(cu)] == 3.0).all()
+    wh, ws = oracle.bf16_to_f32(w_home).astype(np.float64), oracle.bf16_to_f32(w_slots).astype(np.float64)
+    worst = ew.gemm_table("dx", got, ref, oracle.bf16_to_f32(dy).astype(np.float64), cu, E, C,
+                          lambda u, rho: wh[rho] if rho < E else ws[u, rho - E])
+    print(f"input gradient on ragged segments: {worst}")
 
 
 @pytest.mark.parametrize("H, HP", [(256, 128), (512, 256)])
@@ -149,6 +160,9 @@ def test_weight_gradient_on_ragged_segments(lib, poison, H, HP):
                 continue
             err = np.linalg.norm(rh[u, j] - (red0[u, j] + d_slots[u, j])) / np.linalg.norm(d_slots[u, j])
             assert err <= RTOL, (u, j, err)
+    worst = ew.dw_table(gh, rh, d_home, d_slots, oracle.bf16_to_f32(recv).astype(np.float64),
+                        oracle.bf16_to_f32(dy).astype(np.float64), cu, E, C, g0, red0)
+    print(f"weight gradient on ragged segments (H={H}, poison={poison}): {worst}")
 
 
 def test_weight_gradient_on_many_tiny_segments_sm_pairs(lib):
@@ -192,3 +206,6 @@ def test_weight_gradient_on_many_tiny_segments_sm_pairs(lib):
                 continue
             err = np.linalg.norm(rh[u, j] - (red0[u, j] + d_slots[u, j])) / np.linalg.norm(d_slots[u, j])
             assert err <= RTOL, (u, j, err)
+    worst = ew.dw_table(gh, rh, d_home, d_slots, oracle.bf16_to_f32(recv).astype(np.float64),
+                        oracle.bf16_to_f32(dy).astype(np.float64), cu, E_, C_, g0, red0)
+    print(f"weight gradient on tiny segments: {worst}")

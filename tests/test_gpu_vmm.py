@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import elementwise as ew
 import oracle
 import synth
 
@@ -89,6 +90,10 @@ def test_weight_store_aliases_and_shares_the_pool_across_layers(lib):
                 got = oracle.bf16_to_f32(buf.y[torch.from_numpy(rows).to(DEV)].view(torch.int16)
                                          .cpu().numpy().view(np.uint16)).astype(np.float64)
                 assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 2e-2
+                ew.fwd(got, want,
+                       oracle.bf16_to_f32(xr.view(torch.int16).cpu().numpy().view(np.uint16)),
+                       oracle.bf16_to_f32(w[e].view(torch.int16).cpu().numpy().view(np.uint16)),
+                       f"rank {u} row {rho}")
     del slots, home, views
     store.close()
 
