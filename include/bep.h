@@ -108,9 +108,10 @@ int bep_plan(bep_ctx* ctx, const int32_t* topk, int32_t* cu_seqlens, int32_t* sl
 
 /* bep_plan without a context and without any allocation. The pages have no
  * counterpart: this is an addition for callers that cannot call cudaMalloc
- * when they plan -- code running while a stream is captured into a CUDA
- * graph, services whose device memory pool is fixed after warm-up, and
- * embedders that cannot create and keep a bep_ctx.
+ * when they plan -- services whose device memory is handed out once at
+ * start-up and may not grow afterwards, and embedders (plug-ins inside a host
+ * framework that owns the allocator, or code that cannot create and keep a
+ * bep_ctx between calls).
  *   cfg, topk, cu_seqlens, slot_expert, dest, maxvio: as for bep_plan.
  *   device_err [1] int32, device memory (caller-owned): cleared, then receives
  *               this call's BEP_DERR_* bits (what bep_status reports for a
@@ -118,12 +119,14 @@ int bep_plan(bep_ctx* ctx, const int32_t* topk, int32_t* cu_seqlens, int32_t* sl
  * The planner's scratch tables live in a 2 MiB file-scope device array that
  * every GPU loading the library reserves until the process exits; a
  * configuration needing more than 2 MiB (about E * R * ceil(S/256) * 4 bytes
- * plus small tables; the S=8192, E=384, R=8 workload needs 0.4 MiB) returns
+ * plus small tables: the S=8192, E=384, R=8 workload needs 0.4 MiB, and
+ * S=43008 is the largest S that fits at R=8, E=384, B=48) returns
  * BEP_ERR_SIZE before anything is queued. No cudaMalloc, cudaFree or
- * allocating library routine is called. A device's first call looks up the
- * array's device address and sets kernel attributes, so make that first call
- * before any stream capture. All calls share the array: calls whose work
- * overlaps on the GPU race, so the caller serialises them (one stream). */
+ * allocating library routine is called. The first call in a CUDA context
+ * looks up the array's device address and sets kernel attributes, so make
+ * that first call before any stream capture; the lookup is repeated for a new
+ * context (after a device reset, say). All calls share the array: calls whose
+ * work overlaps on the GPU race, so the caller serialises them (one stream). */
 int bep_plan_noalloc(const bep_config* cfg, const int32_t* topk, int32_t* cu_seqlens,
                      int32_t* slot_expert, int32_t* dest, double* maxvio, int32_t* device_err,
                      void* stream);

@@ -500,32 +500,72 @@ cudaError_t launch_plan(const Dims& d, const Workspace& ws, const int32_t* topk,
 // ---------------------------------------------------------------------------
 // Planner entry point that allocates nothing (declared in include/bep.h).
 //
-// Some callers cannot call cudaMalloc when they plan: code that runs while a
-// stream is being captured into a CUDA graph (allocation is not allowed
-// there), services whose memory pool is fixed after warm-up, and embedders
-// that cannot hold a bep_ctx. This variant takes the configuration directly
-// and keeps the planner's scratch tables in a file-scope device array that
-// every GPU loading the library reserves until the process exits.
+// Some callers cannot call cudaMalloc when they plan: services whose device
+// memory is handed out once at start-up and may not grow afterwards, and
+// embedders (plug-ins inside a host framework that owns the allocator, or
+// code that cannot keep a bep_ctx alive between calls). This variant takes the
+// configuration directly and keeps the planner's scratch tables in a
+// file-scope device array that every GPU loading the library reserves until
+// the process exits.
 //
 // Host code must not hand the array's symbol to a kernel: on the host it is a
 // stand-in, not a device address. The device address is fetched with
-// cudaGetSymbolAddress once per device, on that device's first call, which
-// also sets the planner kernels' shared-memory limits. That first call should
-// therefore come before any stream capture. Every call shares the one array:
-// calls whose work overlaps on the GPU (other streams, other threads) race on
-// it and must be serialised by the caller.
-// ---------------------------------------------------------------------------
+// cudaGetSymbolAddress once per CUDA context, on the first call made in that
+// context (normally a device's primary context), which also sets the planner
+// kernels' shared-memory limits. That first call should therefore come
+// before any stream capture. The cache is keyed on the context's unique id,
+// so a device reset or a second context on the same device repeats the
+// set-up instead of reusing an address from a context that no longer exists.
+// Every call shares the one array: calls whose work overlaps on the GPU
+// (other streams, other threads) race on it and must be serialised by the
+// caller.
+#include <cuda.h>
+
 #include <mutex>
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;   // 2 MiB
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxContexts = 64;
 
 __device__ __align__(256) int32_t g_plan_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
+// One entry per CUDA context that has called bep_plan_noalloc: the context's
+// unique id (cuCtxGetId) and the array's device address in it.
+struct NoAllocEntry {
+    unsigned long long ctx_id;
+    int32_t* addr;
+};
 std::mutex g_noalloc_mutex;
-int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+NoAllocEntry g_noalloc[kNoAllocMaxContexts] = {};
+int g_noalloc_n = 0;      // entries in use
+int g_noalloc_next = 0;   // when all are in use, the one to replace next (oldest first)
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The current context's unique id, through the driver entry points the runtime
+// hands out (no link against libcuda). Returns false if there is none yet.
+bool current_ctx_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+                cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !a || !b)
+            return false;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+        get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // Scratch bytes the planner needs for d (the same tables bep_create carves).
 size_t noalloc_bytes(const bep::Dims& d) {
@@ -559,17 +599,36 @@ extern "C" int bep_plan_noalloc(const bep_config* cfg, const int32_t* topk, int3
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BEP_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return BEP_ERR_ARG;
     int32_t* base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-        if (!g_noalloc_addr[dev]) {
+        unsigned long long id = 0;
+        bool known = current_ctx_id(&id);
+        if (known) {
+            for (int i = 0; i < g_noalloc_n; ++i)
+                if (g_noalloc[i].ctx_id == id) base = g_noalloc[i].addr;
+        }
+        if (!base) {
+            // First call in this context: look the array up (this also makes the
+            // device's primary context current if none was), set the kernels up.
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || !p) return BEP_ERR_CUDA;
             if (bep::plan_setup(dev) != cudaSuccess) return BEP_ERR_CUDA;
-            g_noalloc_addr[dev] = static_cast<int32_t*>(p);
+            if (!known && !current_ctx_id(&id)) return BEP_ERR_CUDA;
+            int slot = -1;
+            for (int i = 0; i < g_noalloc_n; ++i)
+                if (g_noalloc[i].ctx_id == id) slot = i;
+            if (slot < 0) {
+                if (g_noalloc_n < kNoAllocMaxContexts) {
+                    slot = g_noalloc_n++;
+                } else {
+                    slot = g_noalloc_next;
+                    g_noalloc_next = (g_noalloc_next + 1) % kNoAllocMaxContexts;
+                }
+            }
+            g_noalloc[slot] = {id, static_cast<int32_t*>(p)};
+            base = g_noalloc[slot].addr;
         }
-        base = g_noalloc_addr[dev];
     }
 
     // The planner's tables, carved from the static array in bep_create's order. Only the
