@@ -122,6 +122,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// After a bounded wait gave up: wait, again with a limit, for a phase this
+// thread knows it started (TMA bytes it armed, MMAs it committed), ignoring
+// the abort flag. Used only on the abort path, so that the kernel frees TMEM
+// and leaves only once its own copies and MMAs have landed (or the limit ran out).
+constexpr uint64_t kDrainNs = 20ull * 1000 * 1000;   // 20 ms
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kDrainNs) return false;
+    return true;
+}
+
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int c0,
                                             int c1) {
     asm volatile(
@@ -326,6 +338,15 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)),
         "h"((uint16_t)3)
+        : "memory");
+}
+
+// The same commit, arriving on CTA 0's barrier only (drain after an abort).
+__device__ __forceinline__ void mma_commit_pair_lead(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)1)
         : "memory");
 }
 
@@ -551,6 +572,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     uint64_t* tempty = bars + 2 * kStages + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    uint64_t* drain = bars + 2 * kStages + 5;   // the MMA thread's last commit after an abort
     int32_t* status = p.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -563,6 +585,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], CF::kEpiWarps);
         }
+        mbar_init(drain, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -582,6 +605,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     const int total = MODE == kDw ? *p.ntiles * p.mtd * NT : *p.ntiles * NT;
     const uint32_t stage_bytes = (uint32_t)(kABytes + b_bytes);
     const int acc_stride = p.tmem_cols / 2;   // two accumulators, power-of-two spaced columns
+    uint32_t pr_s = 0, pr_ph = 0, pr_armed = 0;   // the producer's ring position and stages armed
 
     if (warp == 0) {
         if (lane == 0) {
@@ -605,7 +629,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     for (int c = 0; c < BN / 64; ++c) op(&tmB0, 2 + c, n0 + c * 64, r0);
                 }
             };
-            uint32_t s = 0, ph = 0;
+            uint32_t& s = pr_s;
+            uint32_t& ph = pr_ph;
             bool live = true;
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
@@ -615,6 +640,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    ++pr_armed;
                     uint8_t* a_dst = smA + s * kABytes;
                     uint8_t* b_dst = smB + s * b_bytes;
                     kblock(u, kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
@@ -821,8 +847,24 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 
     __syncthreads();
     if (*s_abort) {
-        // let copies and MMAs that were already issued land before the memory goes away
-        for (int i = 0; i < 100; ++i) __nanosleep(10000);
+        // A wait gave up. Before TMEM and shared memory are released, what was started
+        // lands: the producer waits (bounded) for the full phase of each stage it armed
+        // last (at most the ring), the MMA thread commits once more and waits for that,
+        // and the epilogue warps have already waited for their stores and reduces.
+        if (warp == 0 && lane == 0) {
+            for (uint32_t i = 0; i < pr_armed && i < (uint32_t)kStages; ++i) {
+                if (pr_s == 0) {
+                    pr_s = kStages;
+                    pr_ph ^= 1u;
+                }
+                --pr_s;
+                mbar_drain(&full[pr_s], pr_ph);
+            }
+        } else if (warp == 1 && lane == 0) {
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+        __syncthreads();
     }
     if (warp == 0) {
         tc_fence_after();
@@ -888,6 +930,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
     uint64_t* zpeer = ptail + kPairTails;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kPairBars);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    uint64_t* drain = bars + kPairBars + 1;   // CTA 0's MMA thread's last commit after an abort
     int32_t* status = p.status;
     const uint32_t rank = cluster_rank();
     const bool lead = rank == 0;
@@ -906,6 +949,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
             mbar_init(&ptail[k], 1);
             mbar_init(&zpeer[k], 2);
         }
+        mbar_init(drain, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -937,12 +981,16 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
         *kb_n = (t->rows + kBK - 1) / kBK;
         *tail = t->rows - (*kb_n - 1) * kBK;
     };
+    // the producer's ring position, stages armed and tail stages armed (drain after an abort)
+    uint32_t pr_s = 0, pr_ph = 0, pr_armed = 0, pr_tk = 0;
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (each CTA its own half)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-            uint32_t s = 0, ph = 0, tk = 0;
+            uint32_t& s = pr_s;
+            uint32_t& ph = pr_ph;
+            uint32_t& tk = pr_tk;
             bool live = true;
             for (int unit = cl0; unit < total && live; unit += ncl) {
                 MTile t;
@@ -960,6 +1008,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
                     // the extra rows); CTA 0 then completes the stage's full phase at once
                     const bool tstage = kb == kb_n - 1 && (tail & 15);
                     const int r0 = t.row0 + kb * kBK;
+                    ++pr_armed;
                     if (tstage) {
                         uint64_t* tb = &ptail[tk++ % kPairTails];
                         mbar_arrive_expect_tx(tb, 2 * kPairHalf);
@@ -1117,8 +1166,34 @@ __global__ void __launch_bounds__(kPairThreads, 1) grouped_gemm_dw_pair_kernel(
 
     __syncthreads();
     if (*s_abort) {
-        // let copies and MMAs that were already issued land before the memory goes away
-        for (int i = 0; i < 100; ++i) __nanosleep(10000);
+        // A wait gave up. Before TMEM and shared memory are released, what was started
+        // lands, each wait bounded: each CTA's producer waits for the tail-stage loads it
+        // counted on its own barriers, CTA 0's producer for the full phase of each stage
+        // it armed last (which also counts CTA 1's bytes of those stages), and CTA 0's MMA
+        // thread commits once more and waits for that; the epilogue warps have already
+        // waited for their reduces. CTA 1's loads of a stage CTA 0 never armed cannot be
+        // observed (their bytes count on CTA 0's barrier): the short sleep after the drains
+        // is the fallback bound for those.
+        if (warp == 0 && lane == 0) {
+            for (uint32_t n = pr_tk > kPairTails ? pr_tk - kPairTails : 0; n < pr_tk; ++n)
+                mbar_drain(&ptail[n % kPairTails], (n / kPairTails) & 1u);
+            if (lead) {
+                for (uint32_t i = 0; i < pr_armed && i < (uint32_t)kPairStages; ++i) {
+                    if (pr_s == 0) {
+                        pr_s = kPairStages;
+                        pr_ph ^= 1u;
+                    }
+                    --pr_s;
+                    mbar_drain(&full[pr_s], pr_ph);
+                }
+            }
+        } else if (warp == 1 && lane == 0 && lead) {
+            mma_commit_pair_lead(drain);
+            mbar_drain(drain, 0);
+        }
+        if (threadIdx.x == 0)
+            for (int i = 0; i < 20; ++i) __nanosleep(10000);
+        __syncthreads();
     }
     cluster_sync();   // neither CTA leaves while the other may still signal it or read its tiles
     if (warp == 0) {
