@@ -731,6 +731,32 @@ def run_gpu(args, rank, world, local_rank):
         "small_configs": small,
         "dispatch_pattern_ceiling": fan,
     }
+    dc = result["dispatch_combine"]
+    disp_gbs, comb_gbs = dc["dispatch_gbs"], dc["combine_gbs"]
+    result["summary"] = {
+        "step_tokens_per_s": round(result["value"]),
+        "e2e_tokens_per_s": round(result["e2e"]["value"]),
+        "dispatch_combine_tokens_per_s": round(dc["tokens_per_s"]),
+        "dispatch": {"ms": round(disp_ms, 4), "gbs": round(disp_gbs, 1),
+                     "frac_of_measured_hbm": round(disp_gbs / pk["hbm"], 3),
+                     "frac_of_8000": round(disp_gbs / 8000.0, 3)},
+        "combine": {"ms": round(comb_ms, 4), "gbs": round(comb_gbs, 1),
+                    "frac_of_measured_hbm": round(comb_gbs / pk["hbm"], 3),
+                    "frac_of_8000": round(comb_gbs / 8000.0, 3)},
+        "hbm_peak_gbs": pk["hbm"],
+        "gemm": {"ms": round(gemm_ms, 4), "tflops": round(gemm_tflops, 1),
+                 "frac_of_burst": round(gemm_tflops / pk["bf16"], 3),
+                 "frac_of_sustained": round(gemm_tflops / pk["bf16_sus"], 3)},
+        "step_ms_per_maxvio": {k: v["step_ms"] for k, v in per_target.items()},
+        "dispatch_combine_ms_per_maxvio": {k: round(v["dispatch_ms"] + v["combine_ms"], 4)
+                                           for k, v in per_target.items()},
+        "flatness_dev_from_mean": {"step": result["flatness_dev_from_mean"],
+                                   "forward": result["forward_dev_from_mean"],
+                                   "dispatch_combine": result["dispatch_combine_dev_from_mean"],
+                                   "criterion": 0.10},
+        "dw_ms": (round(bwd["grouped_gemm_dw"]["ms"], 3)
+                  if isinstance(bwd, dict) and "grouped_gemm_dw" in bwd else None),
+    }
     return result
 
 
@@ -779,43 +805,43 @@ class CpuSample:
         R, S, K, E, B, H, Hp = wl.R, wl.S, wl.K, wl.E, wl.B, wl.H, wl.Hp
         C, n, m = S * K, self.N_TOK, self.M_ROWS
         tok_scale = R * S / n
-        t0 = time.perf_counter()
-        p = oracle.plan(self.topk, E, B, wl.mode)
-        t_plan = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        recv = oracle.dispatch(self.x, self.dest)
-        t_disp = (time.perf_counter() - t0) * tok_scale
-        t0 = time.perf_counter()
-        oracle.combine(self.y, self.dest, self.g)
-        t_comb = (time.perf_counter() - t0) * tok_scale
-        t0 = time.perf_counter()
-        oracle.combine_bwd(self.dout, self.dest, self.g)
-        t_bwd = (time.perf_counter() - t0) * tok_scale
-        t0 = time.perf_counter()
-        oracle.gemm_rows(recv[:m], self.w)
-        t_gemm_rows = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        oracle.bf16_to_f32(self.w).astype(np.float64)
-        t_wconv = time.perf_counter() - t0
+        raw = {}
+
+        def timed(name, fn):
+            t0 = time.perf_counter()
+            out = fn()
+            raw[name] = time.perf_counter() - t0
+            return out
+
+        p = timed("plan", lambda: oracle.plan(self.topk, E, B, wl.mode))
+        recv = timed("dispatch", lambda: oracle.dispatch(self.x, self.dest))
+        timed("combine", lambda: oracle.combine(self.y, self.dest, self.g))
+        timed("combine_bwd", lambda: oracle.combine_bwd(self.dout, self.dest, self.g))
+        timed("gemm_rows", lambda: oracle.gemm_rows(recv[:m], self.w))
+        timed("weight_conversion", lambda: oracle.bf16_to_f32(self.w).astype(np.float64))
+        timed("reduce_grad", lambda: oracle.reduce_grad(self.G1, self.red1, self.zero_map))
+        timed("prefetch", lambda: oracle.prefetch(self.w_home1, self.zero_map, self.slots1))
         nseg = int(sum((np.diff(p.cu[u]) > 0).sum() for u in range(R)))
-        t_gemm = max(t_gemm_rows - t_wconv, 0.0) * (R * C / m) + t_wconv * nseg
         used = int((p.slot_expert >= 0).sum())
-        t0 = time.perf_counter()
-        oracle.reduce_grad(self.G1, self.red1, self.zero_map)
-        t_red = (time.perf_counter() - t0) * self.FRAC * used
-        t0 = time.perf_counter()
-        oracle.prefetch(self.w_home1, self.zero_map, self.slots1)
-        t_pref = (time.perf_counter() - t0) * self.FRAC * used
-        step_s = t_plan + t_pref + t_disp + t_gemm + t_comb + t_bwd + t_red
+        # each stage's sample time scaled to one whole step of R*S tokens
+        t_gemm = (max(raw["gemm_rows"] - raw["weight_conversion"], 0.0) * (R * C / m) +
+                  raw["weight_conversion"] * nseg)
+        stages = {"plan": raw["plan"], "prefetch": raw["prefetch"] * self.FRAC * used,
+                  "dispatch": raw["dispatch"] * tok_scale, "gemm": t_gemm,
+                  "combine": raw["combine"] * tok_scale, "combine_bwd": raw["combine_bwd"] * tok_scale,
+                  "reduce_grad": raw["reduce_grad"] * self.FRAC * used}
+        step_s = sum(stages.values())
         return {
-            "value": R * S / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "value": R * S / step_s, "unit": "tokens/s", "kind": "oracle",
             "sample": (f"maxvio-10 routing: plan on all {R * S} tokens; dispatch/combine/"
                        f"combine_bwd on {n} tokens; GEMM on {m} rows + one weight conversion "
                        f"(scaled by {nseg} segments); prefetch/reduce_grad on 1/{self.FRAC} slot "
                        f"(scaled by {used} slots); scaled to one step of {R * S} tokens"),
+            # wall time this sample actually took, and what one whole step would take
+            "sample_seconds": sum(raw.values()),
             "step_seconds_est": step_s,
-            "stages_s": {"plan": t_plan, "prefetch": t_pref, "dispatch": t_disp, "gemm": t_gemm,
-                         "combine": t_comb, "combine_bwd": t_bwd, "reduce_grad": t_red},
+            "scale_to_full_step": step_s / sum(raw.values()),
+            "stages_s": stages,
         }
 
 
@@ -829,31 +855,89 @@ def cpu_samples(steps: int, warmup: int, size: str = "baseline"):
     return out
 
 
-def cpu_baseline_subprocess(steps: int = 1, warmup: int = 0, size: str = "baseline"):
-    """The oracle timing in a fresh single-threaded process (BLAS threads 1)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+def cpu_model() -> str:
+    """The host CPU's model name, as the OS reports it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:   # noqa: BLE001
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline_subprocess(steps: int = 1, warmup: int = 0, size: str = "baseline",
+                            threads: int = 1):
+    """The oracle timing in a fresh process: single-threaded (the oracle as it stands,
+    BLAS threads 1), or on `threads` cores (the same oracle source built with OpenMP,
+    numpy's BLAS on as many threads)."""
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
+    if threads > 1:
+        env["ORACLE_OPENMP"] = "1"
+    else:
+        env.pop("ORACLE_OPENMP", None)
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", size,
                         "--steps", str(steps), "--warmup", str(warmup)], env=env,
                        capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         return [{"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}]
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    for o in out:
+        o["cores"] = threads
+    return out
+
+
+def cpu_baseline():
+    """cpu_baseline of the bench line: the oracle single-threaded (value, cores = 1) and
+    again on every host core (all_cores), one discarded sample before each."""
+    nproc = os.cpu_count() or 1
+    keep = ("value", "unit", "cores", "kind", "sample", "sample_seconds", "step_seconds_est",
+            "scale_to_full_step", "error")
+    one = {k: v for k, v in cpu_baseline_subprocess(1, 1)[0].items() if k in keep}
+    allc = {k: v for k, v in cpu_baseline_subprocess(1, 1, threads=nproc)[0].items()
+            if k in ("value", "cores", "sample_seconds", "step_seconds_est", "error")}
+    allc["build"] = ("the same oracle source built with -fopenmp (per-token loops of dispatch, "
+                     "combine, combine_bwd, prefetch and reduce_grad on every core); numpy BLAS "
+                     "threads = cores for the GEMM rows")
+    one["all_cores"] = allc
+    one["nproc"] = nproc
+    one["cpu_model"] = cpu_model()
+    return one
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the oracle on the host cores, each step one bounded sample."""
+    """The reference arm: the oracle on the host cores, each step one bounded sample.
+    ms_per_step is the wall time a timed step actually took (one sample); value is the
+    sample's throughput scaled to whole steps (each stage by the share of the step it ran)."""
     if rank != 0:
         return None
     res = cpu_baseline_subprocess(args.steps, args.warmup, size="step")
-    vals = [r["value"] for r in res if "value" in r]
-    v = statistics.mean(vals) if vals else None
+    ok = [r for r in res if "value" in r]
+    v = statistics.mean(r["value"] for r in ok) if ok else None
+    wall = statistics.mean(r["sample_seconds"] for r in ok) if ok else None
+    est = statistics.mean(r["step_seconds_est"] for r in ok) if ok else None
     base = res[-1] if res else {}
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": (8 * 8192 / v * 1e3) if v else None, "higher_is_better": True,
+        "ms_per_step": wall * 1e3 if wall else None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32/bf16 (oracle)", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} (R=8, S=8192/rank, E=384, K=8, H=7168, H'=2048, B=48)"},
+        "sample": {"per_step": base.get("sample"),
+                   "measured_seconds_per_step": wall,
+                   "full_step_seconds_est": est,
+                   "scale_to_full_step": (est / wall) if wall else None,
+                   "scaled_tokens_per_s": v},
         "cpu_baseline": {k: base.get(k) for k in ("kind", "cores", "sample")} | {"value": v},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         **({"error": base["error"]} if "error" in base else {}),
@@ -913,9 +997,13 @@ def main():
     res = run_gpu(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            # one discarded sample first: it pays the allocator's first-touch costs
-            res["cpu_baseline"] = {k: v for k, v in cpu_baseline_subprocess(1, 1)[0].items()
-                                   if k in ("value", "unit", "cores", "kind", "sample", "error")}
+            res["cpu_baseline"] = cpu_baseline()
+            cb = res["cpu_baseline"]
+            res["summary"]["cpu_baseline_tokens_per_s"] = {
+                "1_core": cb.get("value"),
+                f"{cb['all_cores'].get('cores')}_cores": cb["all_cores"].get("value")}
+        # the figures the metric names, last on the line
+        res["summary"] = res.pop("summary")
         print(json.dumps(res))
 
 

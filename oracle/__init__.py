@@ -10,6 +10,10 @@ Pieces:
   * ``liboracle.so`` (plain C++, single thread, ``-ffp-contract=off``):
     histogram, maxvio, the planning rule, the plan-validity checker, dispatch,
     combine, combine backward, prefetch and reduce_grad.
+  * ``liboracle_omp.so``: the same source built with ``-fopenmp``, loaded
+    instead when ``ORACLE_OPENMP=1`` is set before the first call. Its per-token
+    loops run on every core and give the same bits; only the CPU baseline's
+    all-core leg uses it.
   * ``grouped_gemm`` (numpy, binary64): the expert GEMM per segment, from
     bf16 inputs, with numpy's matmul as the one library step.
 
@@ -30,7 +34,9 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
-_LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_SERIAL = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
+_LIB = _LIB_OMP if os.environ.get("ORACLE_OPENMP") == "1" else _LIB_SERIAL
 _lock = threading.Lock()
 _lib = None
 
@@ -46,15 +52,23 @@ ERRORS = {
 }
 
 
-def build(force: bool = False) -> str:
-    """Compile ``liboracle.so`` with the host C++ compiler."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
+def _compile(lib: str, openmp: bool, force: bool) -> str:
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
-               "-o", tmp, _SRC]
+               "-Wno-unknown-pragmas"] + (["-fopenmp"] if openmp else []) + ["-o", tmp, _SRC]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB)
-    return _LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build(force: bool = False, openmp: bool | None = None) -> str:
+    """Compile the oracle with the host C++ compiler: the single-threaded
+    ``liboracle.so`` (openmp=False), the OpenMP ``liboracle_omp.so`` (True), or
+    the one this process loads (None)."""
+    if openmp is None:
+        openmp = _LIB == _LIB_OMP
+    return _compile(_LIB_OMP if openmp else _LIB_SERIAL, openmp, force)
 
 
 def _load():

@@ -28,7 +28,11 @@
 // which is independent of the rule.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared (no FMA contraction,
-// so every fused multiply-add below is the explicit std::fma call).
+// so every fused multiply-add below is the explicit std::fma call). The same
+// source built with -fopenmp as well runs the per-token loops of the data
+// stages on every core (the "omp parallel for" lines below; without -fopenmp
+// the compiler ignores them). Each iteration writes its own outputs only, so
+// both builds give the same bits; the CPU baseline times both.
 
 #include <algorithm>
 #include <cmath>
@@ -415,6 +419,7 @@ int oracle_check_plan(int R, int E, int B, int K, int S, int mode, const int32_t
 void oracle_dispatch(const uint16_t* x, const int32_t* dest, int R, int S, int K, int H,
                      uint16_t* recv) {
     int64_t ntok = (int64_t)R * S;
+#pragma omp parallel for schedule(static)
     for (int64_t tok = 0; tok < ntok; ++tok)
         for (int k = 0; k < K; ++k) {
             int64_t d = dest[tok * K + k];
@@ -427,6 +432,7 @@ void oracle_dispatch(const uint16_t* x, const int32_t* dest, int R, int S, int K
 void oracle_combine(const uint16_t* y, const int32_t* dest, const float* gates, int R, int S,
                     int K, int D, uint16_t* out) {
     int64_t ntok = (int64_t)R * S;
+#pragma omp parallel for schedule(static)
     for (int64_t tok = 0; tok < ntok; ++tok)
         for (int c = 0; c < D; ++c) {
             float acc = 0.0f;
@@ -443,6 +449,7 @@ void oracle_combine(const uint16_t* y, const int32_t* dest, const float* gates, 
 void oracle_combine_bwd(const uint16_t* dout, const int32_t* dest, const float* gates, int R,
                         int S, int K, int D, uint16_t* dy) {
     int64_t ntok = (int64_t)R * S;
+#pragma omp parallel for schedule(static)
     for (int64_t tok = 0; tok < ntok; ++tok)
         for (int k = 0; k < K; ++k) {
             int64_t d = dest[tok * K + k];
@@ -461,6 +468,7 @@ void oracle_combine_bwd(const uint16_t* dout, const int32_t* dest, const float* 
 void oracle_dispatch_bwd(const uint16_t* drecv, const int32_t* dest, int R, int S, int K, int H,
                          uint16_t* dx) {
     int64_t ntok = (int64_t)R * S;
+#pragma omp parallel for schedule(static)
     for (int64_t tok = 0; tok < ntok; ++tok)
         for (int c = 0; c < H; ++c) {
             float acc = 0.0f;
@@ -477,6 +485,7 @@ void oracle_dispatch_bwd(const uint16_t* drecv, const int32_t* dest, int R, int 
 void oracle_combine_dgates(const uint16_t* dout, const uint16_t* y, const int32_t* dest, int R,
                            int S, int K, int D, double* dg) {
     int64_t ntok = (int64_t)R * S;
+#pragma omp parallel for schedule(static)
     for (int64_t tok = 0; tok < ntok; ++tok)
         for (int k = 0; k < K; ++k) {
             int64_t d = dest[tok * K + k];
@@ -495,8 +504,14 @@ void oracle_prefetch(const uint16_t* w_home, const int32_t* slot_expert, int R, 
         for (int j = 0; j < B; ++j) {
             int e = slot_expert[(int64_t)u * B + j];
             if (e < 0) continue;
-            std::memcpy(w_slots + ((int64_t)u * B + j) * HHp, w_home + (int64_t)e * HHp,
-                        sizeof(uint16_t) * (size_t)HHp);
+            uint16_t* dst = w_slots + ((int64_t)u * B + j) * HHp;
+            const uint16_t* src = w_home + (int64_t)e * HHp;
+            // the row in 64 KiB pieces (one piece per iteration of the parallel build)
+            const int64_t piece = 32768;
+#pragma omp parallel for schedule(static)
+            for (int64_t i = 0; i < HHp; i += piece)
+                std::memcpy(dst + i, src + i,
+                            sizeof(uint16_t) * (size_t)(HHp - i < piece ? HHp - i : piece));
         }
 }
 
@@ -514,6 +529,7 @@ void oracle_reduce_grad(float* G, float* red, const int32_t* slot_expert, int R,
                 if (slot_expert[(int64_t)r * B + j] != e) continue;
                 float* g = G + (int64_t)e * HHp;
                 float* s = red + ((int64_t)r * B + j) * HHp;
+#pragma omp parallel for schedule(static)
                 for (int64_t i = 0; i < HHp; ++i) {
                     g[i] = g[i] + s[i];
                     s[i] = 0.0f;

@@ -774,3 +774,48 @@ def test_sampled_gemm_helpers_agree_with_the_whole_gemm():
         e = oracle.weight_row_of(rho, i // C, E, ref.slot_expert)
         np.testing.assert_allclose(oracle.gemm_rows(recv[i:i + 1], w_home[e])[0], y[i],
                                    rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- the OpenMP build
+def test_openmp_build_gives_the_same_bits(tmp_path):
+    """The CPU baseline's all-core leg loads the same oracle source built with
+    -fopenmp: its data stages must give exactly the single-threaded bits."""
+    import subprocess
+    import sys
+    try:
+        oracle.build(openmp=True)
+    except Exception as exc:   # noqa: BLE001
+        pytest.skip(f"no OpenMP compiler here: {exc}")
+    topk, p, x, g, y = _small_problem(S=300, K=4, H=48, D=40)
+    w_home = synth.weights_host((16, 6, 10), 3)
+    red0 = synth.normal_host((2, 8, 6, 10), 4, 1.0)
+    np.savez(tmp_path / "in.npz", dest=p.dest, x=x, g=g, y=y, se=p.slot_expert, w_home=w_home,
+             red0=red0)
+    code = f"""
+import numpy as np, sys
+sys.path.insert(0, {os.path.dirname(os.path.dirname(os.path.abspath(__file__)))!r})
+import oracle
+d = np.load({str(tmp_path / 'in.npz')!r})
+g_home = np.zeros((16, 6, 10), np.float32); red = d['red0'].copy()
+oracle.reduce_grad(g_home, red, d['se'])
+np.savez({str(tmp_path / 'out.npz')!r},
+         recv=oracle.dispatch(d['x'], d['dest']), out=oracle.combine(d['y'], d['dest'], d['g']),
+         dy=oracle.combine_bwd(d['x'][..., :40], d['dest'], d['g']),
+         dx=oracle.dispatch_bwd(oracle.dispatch(d['x'], d['dest']), d['dest']),
+         slots=oracle.prefetch(d['w_home'], d['se'], np.zeros((2, 8, 6, 10), np.uint16)),
+         g_home=g_home, red=red)
+"""
+    env = dict(os.environ, ORACLE_OPENMP="1", OMP_NUM_THREADS="4")
+    subprocess.run([sys.executable, "-c", code], env=env, check=True)
+    got = np.load(tmp_path / "out.npz")
+    g_home = np.zeros((16, 6, 10), np.float32)
+    red = red0.copy()
+    oracle.reduce_grad(g_home, red, p.slot_expert)
+    recv = oracle.dispatch(x, p.dest)
+    want = dict(recv=recv, out=oracle.combine(y, p.dest, g),
+                dy=oracle.combine_bwd(x[..., :40].copy(), p.dest, g),
+                dx=oracle.dispatch_bwd(recv, p.dest),
+                slots=oracle.prefetch(w_home, p.slot_expert, np.zeros((2, 8, 6, 10), np.uint16)),
+                g_home=g_home, red=red)
+    for k, v in want.items():
+        np.testing.assert_array_equal(got[k], v, err_msg=k)
