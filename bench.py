@@ -143,19 +143,30 @@ def run_inference(bep, synth, w_home, stream, dev, reps):
     gates = torch.from_numpy(synth.gates_host(R, S, K, 11)).to(dev)
     w_slots = torch.zeros((R, B, H, Hp), dtype=torch.bfloat16, device=dev)
     res = {"workload": f"{name} (R={R}, S={S}/rank, E={E}, K={K}, H={H}, H'={Hp}, B={B}, inference)"}
+    pk = peaks()
     for target in synth.MAXVIO_TARGETS[name]:
         topk = torch.from_numpy(synth.routing(wl, target, 0)).to(dev)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        # events around each call: plan | prefetch | dispatch | GEMM | combine
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
         for i in range(reps + 1):
+            e = ev[i - 1] if i > 0 else None
+            if e:
+                e[0].record(stream)
             bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio, stream)
+            if e:
+                e[1].record(stream)
             bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+            if e:
+                e[2].record(stream)
             bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
-            if i > 0:
-                ev[i - 1][0].record(stream)
+            if e:
+                e[3].record(stream)
             bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y, stream)
-            if i > 0:
-                ev[i - 1][1].record(stream)
+            if e:
+                e[4].record(stream)
             bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+            if e:
+                e[5].record(stream)
         torch.cuda.synchronize()
         st = bep.bep_status(ctx, stream)
         if st:
@@ -166,13 +177,24 @@ def run_inference(bep, synth, w_home, stream, dev, reps):
         nonempty = (cu[:, 1:E + 1] > cu[:, :E]).cpu()
         home = (torch.arange(E) // (E // R))[None, :] == torch.arange(R)[:, None]
         overflow = int((nonempty & ~home).sum().item())
-        ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        st_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(5)]
+        ms = st_ms[3]
         byts = nseg * H * Hp * 2 + R * S * K * (H + Hp) * 2
+        used = int((buf.slot_expert >= 0).sum().item())
+        moved = {"prefetch": used * 2 * H * Hp * 2,
+                 "dispatch": R * S * H * 2 + R * S * K * H * 2 + R * S * K * 4,
+                 "combine": R * S * K * Hp * 2 + R * S * Hp * 2 + R * S * K * 8}
+        stage = {}
+        for j, nm in ((1, "prefetch"), (2, "dispatch"), (4, "combine")):
+            gbs = moved[nm] / (st_ms[j] * 1e-3) / 1e9
+            stage[nm] = {"ms": round(st_ms[j], 4), "gbs": round(gbs, 1),
+                         "frac_hbm": round(gbs / pk["hbm"], 3)}
         res[str(target)] = {"maxvio": round(float(buf.maxvio.item()), 4), "segments": nseg,
                             "gemm_ms": ms, "gemm_gbs": byts / (ms * 1e-3) / 1e9,
-                            "frac_hbm": byts / (ms * 1e-3) / 1e9 / peaks()["hbm"],
+                            "frac_hbm": byts / (ms * 1e-3) / 1e9 / pk["hbm"],
                             "tflops": 2.0 * R * S * K * H * Hp / (ms * 1e-3) / 1e12,
-                            "overflow_segments": overflow}
+                            "overflow_segments": overflow, "plan_ms": round(st_ms[0], 4),
+                            "replicas": used, **stage}
     del ctx, buf, x, w_slots
     torch.cuda.empty_cache()
     return res

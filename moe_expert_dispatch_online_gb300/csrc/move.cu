@@ -13,7 +13,10 @@
 // Every row moves as 16-byte vectors. One warp owns one token: it reads the
 // token's K destinations (lane k holds dest k), then streams the row with
 // several independent 16-byte loads in flight per lane. Grids are a multiple
-// of the SM count; warps stride over tokens.
+// of the SM count; warps stride over tokens. When there are fewer tokens than
+// warps in the grid (small batches), each row is cut into `pieces` runs of
+// 32*U vectors and a warp owns one (token, piece) item, so every warp of the
+// grid has rows in flight.
 
 #include <cuda_bf16.h>
 
@@ -71,25 +74,47 @@ __device__ __forceinline__ int load_dest(const int32_t* __restrict__ dest, int64
 
 // ----------------------------------------------------------------------------- dispatch
 // recv[dest[tok, k], :] = x[tok, :]
+// The vectors [*v_lo, *v_hi) of item `item`'s row piece, for rows of nvec vectors cut
+// into `pieces` runs of whole 32*U-vector steps; returns the item's token.
+template <int U>
+__device__ __forceinline__ int64_t piece_of(int64_t item, int pieces, int nvec, int* v_lo,
+                                            int* v_hi) {
+    if (pieces == 1) {
+        *v_lo = 0;
+        *v_hi = nvec;
+        return item;
+    }
+    const int64_t tok = item / pieces;
+    const int piece = (int)(item - tok * pieces);
+    const int steps = (nvec + 32 * U - 1) / (32 * U);
+    const int per = (steps + pieces - 1) / pieces;
+    *v_lo = min(nvec, piece * per * 32 * U);
+    *v_hi = min(nvec, (piece + 1) * per * 32 * U);
+    return tok;
+}
+
 template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ dest,
                                                             uint4* __restrict__ recv, int64_t ntok,
                                                             int K, int nvec, int64_t nrows,
-                                                            int32_t* status) {
+                                                            int pieces, int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t tok = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < ntok;
-         tok += nwarps) {
+    const int64_t nitem = ntok * pieces;
+    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < nitem;
+         item += nwarps) {
+        int v_lo, v_hi;
+        const int64_t tok = piece_of<U>(item, pieces, nvec, &v_lo, &v_hi);
         unsigned okmask;
         const int dl = load_dest(dest, tok, K, nrows, &okmask, status);
         const uint4* src = x + tok * nvec;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int v0 = v_lo; v0 < v_hi; v0 += 32 * U) {
             uint4 val[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * 32 + lane;
-                if (v < nvec) val[u] = ld_stream(src + v);
+                if (v < v_hi) val[u] = ld_stream(src + v);
             }
             for (int k = 0; k < K; ++k) {
                 const int dk = __shfl_sync(0xffffffffu, dl, k);
@@ -98,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restr
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + u * 32 + lane;
-                    if (v < nvec) dst[v] = val[u];
+                    if (v < v_hi) dst[v] = val[u];
                 }
             }
         }
@@ -114,21 +139,28 @@ __device__ __forceinline__ float combine_step(float g, float v, float acc) {
     return kWeighted ? __fmaf_rn(g, v, acc) : __fadd_rn(acc, v);
 }
 
-template <int U, bool kWeighted>
+// kPieces: rows cut into pieces (small batches of long rows); without it a warp owns
+// whole rows, which measured faster for this gather wherever rows are short or tokens
+// many (the instance without pieces is the one combine always uses).
+template <int U, bool kWeighted, bool kPieces>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ y,
                                                            const int32_t* __restrict__ dest,
                                                            const float* __restrict__ gates,
                                                            uint4* __restrict__ out, int64_t ntok,
                                                            int K, int nvec, int64_t nrows,
-                                                           int32_t* status) {
+                                                           int pieces, int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t tok = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < ntok;
-         tok += nwarps) {
+    const int64_t nitem = kPieces ? ntok * pieces : ntok;
+    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < nitem;
+         item += nwarps) {
+        int v_lo = 0, v_hi = nvec;
+        int64_t tok = item;
+        if (kPieces) tok = piece_of<U>(item, pieces, nvec, &v_lo, &v_hi);
         unsigned okmask;
         const int dl = load_dest(dest, tok, K, nrows, &okmask, status);
         const float gl = (kWeighted && lane < K) ? gates[tok * K + lane] : 1.0f;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int v0 = v_lo; v0 < v_hi; v0 += 32 * U) {
             float acc[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -148,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                     const int v = v0 + u * 32 + lane;
                     q0[u] = make_uint4(0, 0, 0, 0);
                     q1[u] = make_uint4(0, 0, 0, 0);
-                    if (v < nvec) {
+                    if (v < v_hi) {
                         if (ok0) q0[u] = ld_stream(y + (int64_t)d0 * nvec + v);
                         if (ok1) q1[u] = ld_stream(y + (int64_t)d1 * nvec + v);
                     }
@@ -172,7 +204,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + u * 32 + lane;
                     uint4 q = make_uint4(0, 0, 0, 0);
-                    if (v < nvec && ok0) q = ld_stream(y + (int64_t)d0 * nvec + v);
+                    if (v < v_hi && ok0) q = ld_stream(y + (int64_t)d0 * nvec + v);
                     float f[8];
                     bf16x8_to_f32(q, f);
 #pragma unroll
@@ -182,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * 32 + lane;
-                if (v < nvec) out[tok * nvec + v] = f32x8_to_bf16(acc[u]);
+                if (v < v_hi) out[tok * nvec + v] = f32x8_to_bf16(acc[u]);
             }
         }
     }
@@ -190,28 +222,35 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 
 // ----------------------------------------------------------------------------- combine backward
 // dy[dest[tok,k], c] = bf16_rne(g[tok,k] * dout[tok, c])
-template <int U>
+// kPieces as for combine_kernel: the instance with (token, piece) items measured faster at
+// large batches and at every size for long rows; whole rows per warp (the other instance)
+// measured faster for short rows in small batches (about 4,000-8,000 tokens of 2048).
+template <int U, bool kPieces>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __restrict__ dout,
                                                                const int32_t* __restrict__ dest,
                                                                const float* __restrict__ gates,
                                                                uint4* __restrict__ dy, int64_t ntok,
                                                                int K, int nvec, int64_t nrows,
-                                                               int32_t* status) {
+                                                               int pieces, int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t tok = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tok < ntok;
-         tok += nwarps) {
+    const int64_t nitem = kPieces ? ntok * pieces : ntok;
+    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < nitem;
+         item += nwarps) {
+        int v_lo = 0, v_hi = nvec;
+        int64_t tok = item;
+        if (kPieces) tok = piece_of<U>(item, pieces, nvec, &v_lo, &v_hi);
         unsigned okmask;
         const int dl = load_dest(dest, tok, K, nrows, &okmask, status);
         const float gl = lane < K ? gates[tok * K + lane] : 0.0f;
         const uint4* src = dout + tok * nvec;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int v0 = v_lo; v0 < v_hi; v0 += 32 * U) {
             float f[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * 32 + lane;
                 uint4 q = make_uint4(0, 0, 0, 0);
-                if (v < nvec) q = ld_stream(src + v);
+                if (v < v_hi) q = ld_stream(src + v);
                 bf16x8_to_f32(q, f[u]);
             }
             for (int k = 0; k < K; ++k) {
@@ -225,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                     float p[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) p[i] = __fmul_rn(gk, f[u][i]);
-                    if (v < nvec) dst[v] = f32x8_to_bf16(p);
+                    if (v < v_hi) dst[v] = f32x8_to_bf16(p);
                 }
             }
         }
@@ -456,15 +495,27 @@ int grid_for(int64_t work_warps, int num_sms) {
     return (int)g;
 }
 
+// Row pieces per token: every 32*U-vector step of a row is an item of its own when the
+// grid has more warps than there are tokens and rows are at least 4 steps long
+// (4,096 tokens of 7168 bf16: dispatch 0.101 -> 0.091 ms, dispatch backward 0.105 ->
+// 0.091 ms on one GB300); otherwise 1 (at 2 steps per row, pieces measured no better).
+template <int U>
+int pieces_for(int64_t ntok, int nvec, int num_sms) {
+    const int64_t warps = (int64_t)num_sms * kCtasPerSm * (kThreads / 32);
+    const int steps = (nvec + 32 * U - 1) / (32 * U);
+    return (ntok < warps && steps >= 4) ? steps : 1;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const Dims& d, const Workspace& ws, const uint16_t* x,
                             const int32_t* dest, uint16_t* recv, int num_sms, cudaStream_t st) {
     const int64_t ntok = (int64_t)d.R * d.S;
     if (ntok == 0) return cudaSuccess;
-    dispatch_kernel<4><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+    const int pieces = pieces_for<4>(ntok, d.H / 8, num_sms);
+    dispatch_kernel<4><<<grid_for(ntok * pieces, num_sms), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(x), dest, reinterpret_cast<uint4*>(recv), ntok, d.K,
-        d.H / 8, (int64_t)d.R * d.C, ws.status);
+        d.H / 8, (int64_t)d.R * d.C, pieces, ws.status);
     return cudaGetLastError();
 }
 
@@ -473,9 +524,11 @@ cudaError_t launch_combine(const Dims& d, const Workspace& ws, const uint16_t* y
                            int num_sms, cudaStream_t st) {
     const int64_t ntok = (int64_t)d.R * d.S;
     if (ntok == 0) return cudaSuccess;
-    combine_kernel<4, true><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+    // whole rows per warp: at 4,096 tokens and D = 2048, two pieces per row measured 7%
+    // slower than one (each piece reloads the token's K destinations and gates)
+    combine_kernel<4, true, false><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(y), dest, gates, reinterpret_cast<uint4*>(out), ntok, d.K,
-        D / 8, (int64_t)d.R * d.C, ws.status);
+        D / 8, (int64_t)d.R * d.C, 1, ws.status);
     return cudaGetLastError();
 }
 
@@ -494,9 +547,15 @@ cudaError_t launch_dispatch_bwd(const Dims& d, const Workspace& ws, const uint16
                                 const int32_t* dest, uint16_t* dx, int num_sms, cudaStream_t st) {
     const int64_t ntok = (int64_t)d.R * d.S;
     if (ntok == 0) return cudaSuccess;
-    combine_kernel<4, false><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(drecv), dest, nullptr, reinterpret_cast<uint4*>(dx), ntok,
-        d.K, d.H / 8, (int64_t)d.R * d.C, ws.status);
+    const int pieces = pieces_for<4>(ntok, d.H / 8, num_sms);
+    if (pieces > 1)
+        combine_kernel<4, false, true><<<grid_for(ntok * pieces, num_sms), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(drecv), dest, nullptr, reinterpret_cast<uint4*>(dx), ntok,
+            d.K, d.H / 8, (int64_t)d.R * d.C, pieces, ws.status);
+    else
+        combine_kernel<4, false, false><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(drecv), dest, nullptr, reinterpret_cast<uint4*>(dx), ntok,
+            d.K, d.H / 8, (int64_t)d.R * d.C, 1, ws.status);
     return cudaGetLastError();
 }
 
@@ -505,9 +564,16 @@ cudaError_t launch_combine_bwd(const Dims& d, const Workspace& ws, const uint16_
                                int num_sms, cudaStream_t st) {
     const int64_t ntok = (int64_t)d.R * d.S;
     if (ntok == 0) return cudaSuccess;
-    combine_bwd_kernel<4><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(dout), dest, gates, reinterpret_cast<uint4*>(dy), ntok, d.K,
-        D / 8, (int64_t)d.R * d.C, ws.status);
+    const int pieces = pieces_for<4>(ntok, D / 8, num_sms);
+    const int64_t warps = (int64_t)num_sms * kCtasPerSm * (kThreads / 32);
+    if (pieces > 1 || ntok >= warps)
+        combine_bwd_kernel<4, true><<<grid_for(ntok * pieces, num_sms), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(dout), dest, gates, reinterpret_cast<uint4*>(dy), ntok,
+            d.K, D / 8, (int64_t)d.R * d.C, pieces, ws.status);
+    else
+        combine_bwd_kernel<4, false><<<grid_for(ntok, num_sms), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(dout), dest, gates, reinterpret_cast<uint4*>(dy), ntok,
+            d.K, D / 8, (int64_t)d.R * d.C, 1, ws.status);
     return cudaGetLastError();
 }
 

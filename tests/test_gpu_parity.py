@@ -555,3 +555,36 @@ def test_grouped_gemm_tile_shapes(lib, R, S, K, E, B, mode, H, Hp):
         G = E // R
         assert any(ref.cu[u, e + 1] > ref.cu[u, e] for u in range(R) for e in range(E)
                    if e // G != u), "the case must exercise overflow rows"
+
+
+def test_token_kernels_bit_exact_at_inference_size(lib):
+    """S=512 per rank (4,096 tokens, fewer than the grid's warps): the token kernels cut
+    each row into pieces, one warp per (token, piece). Dispatch and dispatch backward
+    (H=7168: 7 pieces), combine and combine backward (H'=2048: 2 pieces) are compared
+    with the oracle on every token, bit for bit."""
+    bep = lib
+    name = "infer_r8_e384_b4"
+    wl = synth.WORKLOADS[name]
+    ref = oracle_plan(name, 1.0, 0)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), routing(name, 1.0, 0))
+    assert_plan_equal(buf, ref)
+    x = synth.tokens_host((wl.R, wl.S, wl.H), 601)
+    recv = Guarded((wl.R * wl.C, wl.H), torch.bfloat16)
+    bep.bep_dispatch(ctx, dev_u16(x), buf.dest, recv.t)
+    y = synth.tokens_host((wl.R * wl.C, wl.Hp), 602)
+    gates = synth.gates_host(wl.R, wl.S, wl.K, 603)
+    out = Guarded((wl.R, wl.S, wl.Hp), torch.bfloat16)
+    bep.bep_combine(ctx, dev_u16(y), buf.dest, torch.from_numpy(gates).to(DEV), out.t)
+    dout = synth.tokens_host((wl.R, wl.S, wl.Hp), 604)
+    dy = Guarded((wl.R * wl.C, wl.Hp), torch.bfloat16)
+    bep.bep_combine_bwd(ctx, dev_u16(dout), buf.dest, torch.from_numpy(gates).to(DEV), dy.t)
+    drecv = synth.tokens_host((wl.R * wl.C, wl.H), 605)
+    dx = Guarded((wl.R, wl.S, wl.H), torch.bfloat16)
+    bep.bep_dispatch_bwd(ctx, dev_u16(drecv), buf.dest, dx.t)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    assert recv.intact() and out.intact() and dy.intact() and dx.intact()
+    np.testing.assert_array_equal(host_u16(recv.t), oracle.dispatch(x, ref.dest))
+    np.testing.assert_array_equal(host_u16(out.t), oracle.combine(y, ref.dest, gates))
+    np.testing.assert_array_equal(host_u16(dy.t), oracle.combine_bwd(dout, ref.dest, gates))
+    np.testing.assert_array_equal(host_u16(dx.t), oracle.dispatch_bwd(drecv, ref.dest))
