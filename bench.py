@@ -36,7 +36,7 @@ METRIC = "dispatch+combine tokens/s and HBM GB/s vs peak, maxvio 0.2-20, 1 GB300
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the forward
 # grouped GEMM, from one ncu capture of this bench at full size (mean over the four
 # routings). Must be reset to None whenever that kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 24.68e9}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 25.16e9}
 
 # Input sets the end-to-end loop keeps on the device: uploads run up to this many steps
 # ahead of compute (1.5 GB per set at the S=8192, E=384 workload, 18 GB in all).
@@ -434,6 +434,53 @@ def run_gpu(args, rank, world, local_rank):
         del drecv, dx
         torch.cuda.empty_cache()
 
+    # ---- the forward with prefetch_weight on a side stream beside the dispatch: the slots
+    # must be filled before the GEMM only, and the dispatch does not touch them. Both
+    # chains are timed back to back per routing (plan -> prefetch | dispatch -> GEMM ->
+    # combine), L2 holding no inputs (tens of GB move per chain).
+    overlap = None
+    if not args.no_backward:
+        side = torch.cuda.Stream(device=dev)
+        n_ov = max(2, min(args.steps, 8))
+        ser, ovl = {}, {}
+        for j, topk in enumerate(topks):
+            key = "zipf1.2" if targets[j] is None else f"{targets[j]:g}"
+            ts_s, ts_o = [], []
+            for i in range(n_ov + 1):
+                for mode, ts in (("serial", ts_s), ("overlap", ts_o)):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    planned = torch.cuda.Event()
+                    filled = torch.cuda.Event()
+                    a.record(stream)
+                    bep.bep_plan(ctx, topk, buf.cu_seqlens, buf.slot_expert, buf.dest, buf.maxvio,
+                                 stream)
+                    if mode == "serial":
+                        bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, stream)
+                        bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+                    else:
+                        planned.record(stream)
+                        side.wait_event(planned)
+                        bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots, side)
+                        filled.record(side)
+                        bep.bep_dispatch(ctx, x, buf.dest, buf.recv, stream)
+                        stream.wait_event(filled)
+                    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y,
+                                         stream)
+                    bep.bep_combine(ctx, buf.y, buf.dest, gates, buf.out, stream)
+                    b.record(stream)
+                    if i > 0:
+                        ts.append((a, b))
+            torch.cuda.synchronize()
+            ser[key] = statistics.mean(a.elapsed_time(b) for a, b in ts_s)
+            ovl[key] = statistics.mean(a.elapsed_time(b) for a, b in ts_o)
+        st = bep.bep_status(ctx, stream)
+        if st:
+            raise RuntimeError(f"device status {st}: {bep.strerror(st)}")
+        overlap = {"forward_ms_serial": {k: round(v, 4) for k, v in ser.items()},
+                   "forward_ms_prefetch_on_side_stream": {k: round(v, 4) for k, v in ovl.items()},
+                   "saving_ms_mean": round(statistics.mean(ser[k] - ovl[k] for k in ser), 4),
+                   "repeats": n_ov}
+
     # ---- dispatch + combine under a 32-SM budget (the pages' comm-SM setting)
     comm32 = None
     if not args.no_backward:
@@ -745,6 +792,7 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": 12 * args.steps,
         "clocks": clocks,
         "backward": bwd,
+        "prefetch_overlap": overlap,
         "comm_sms_32": comm32,
         "vm_group_gemm": vmg,
         "combine_d_h": comb_h,
