@@ -632,8 +632,17 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             uint32_t& s = pr_s;
             uint32_t& ph = pr_ph;
             bool live = true;
-            for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x) {
+            // FWD: a CTA's odd units walk K from the end. The CTAs stay close to lockstep
+            // (every unit has the same K length), so successive waves of units alternate
+            // direction, and the units of a segment that straddles two waves start where
+            // the earlier wave ended: on the weight and row tiles most recently loaded,
+            // which are still in L2, instead of on the first ones, long evicted. At the
+            // S=8192, E=384 routings this took 1-2 GB (7-8%) off the DRAM traffic per launch
+            // at the same time; for DX it measured 1.8% slower, so DX keeps one direction.
+            int it = 0;
+            for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
+                const bool rev = MODE == kFwd && (it & 1);
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
@@ -643,7 +652,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     ++pr_armed;
                     uint8_t* a_dst = smA + s * kABytes;
                     uint8_t* b_dst = smB + s * b_bytes;
-                    kblock(u, kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
+                    kblock(u, rev ? u.kb_n - 1 - kb : kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
                         uint8_t* dst = piece < 2 ? a_dst + piece * kBChunkBytes
                                                  : b_dst + (piece - 2) * kBChunkBytes;
                         tma_load_2d(m, &full[s], dst, c0, c1);
