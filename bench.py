@@ -783,9 +783,12 @@ def run_gpu(args, rank, world, local_rank):
         "dispatch_combine_dev_from_mean": flat_dev(
             [v["dispatch_ms"] + v["combine_ms"] for v in per_target.values()]),
         "forward_dev_from_mean": flat_dev([v["forward_ms"] for v in per_target.values()]),
+        # The timed region is K steps of about 12 ms (a fraction of a second), not a seconds-long
+        # loop, so the burst peak is the one that applies; the sustained figure rides along.
         "roofline": {"kernel": "grouped_gemm", "bound": "tensor", "achieved": gemm_tflops,
-                     "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_sus"],
-                     "peak_source": f"{pk['src']} bf16 sustained (kernel timed inside a long step)",
+                     "peak": pk["bf16"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16"],
+                     "peak_source": f"{pk['src']} bf16 burst (the timed region lasts under a second)",
+                     "frac_of_sustained": gemm_tflops / pk["bf16_sus"],
                      "traffic": traffic},
         "e2e": {"value": world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
