@@ -414,6 +414,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // seg_mode == 2: as 1, plus an entry with rows = 0 for every expert whose home segment
 //   (rank e / (E/R), row e) is empty, so that an overwriting DW writes its zeros; a
 //   non-empty home row on any other rank refuses the table.
+// DW entries are merged the same way, long against short: every unit of a segment adds
+//   (or writes) a whole 256 KB gradient tile, but runs MMAs only over the segment's rows,
+//   so a segment of a few hundred rows is all gradient traffic and a long one all MMAs.
+//   Skewed routings have both (at maxvio 10 on the S=8192, E=384 workload, 136 of 372
+//   segments hold fewer than 256 rows); merged evenly, CTAs on short segments move
+//   gradients while the others keep the tensor pipes busy.
+constexpr int kDwShortRows = 1024;
+
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
     __shared__ int s_warp[33];
@@ -440,21 +448,26 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         if (seg_mode) return b > a ? 1 : 0;
         return (b - a + kBM - 1) / kBM;
     };
+    // FWD/DX: a segment of three or more m-tiles is long; DW: one of kDwShortRows rows or more
+    auto is_long = [&](int n, int l) { return seg_mode ? l >= kDwShortRows : n > 2; };
+    // the merge is for the accumulating DW only: the overwriting one reads no gradient, its
+    // short segments' units are light, and there merging measured no faster
     int nlong = 0, nshort = 0;
     for (int i = lo; i < hi; ++i) {
-        int s, l;
+        int s = 0, l = 0;
         const int n = tiles_of(i, &s, &l);
-        if (n > 2) nlong += n;
+        if (is_long(n, l)) nlong += n;
         else nshort += n;
     }
     int Nl = 0, Ns = 0;
     int run_l = block_exclusive_scan(nlong, s_warp, &Nl);
     int run_s = block_exclusive_scan(nshort, s_warp, &Ns);
     const int total = Nl + Ns;
-    // merge only where the short tiles are a fifth or more of the work (skewed inference
-    // batches); with a few short tiles among many long ones (training) spreading them
-    // only moved weight rows out of L2 early, so the order stays plain
-    const bool mix = Nl > 0 && Ns > 0 && 4 * (int64_t)Ns >= Nl;
+    // FWD/DX: merge only where the short tiles are a fifth or more of the work (skewed
+    // inference batches); with a few short tiles among many long ones (training) spreading
+    // them only moved weight rows out of L2 early, so the order stays plain. DW: merge
+    // whenever both kinds are present.
+    const bool mix = Nl > 0 && Ns > 0 && seg_mode != 2 && (seg_mode == 1 || 4 * (int64_t)Ns >= Nl);
     // one inconsistent segment anywhere refuses the whole table: nothing is computed
     const bool ok = !__syncthreads_or(bad) && total <= d.max_tiles;
     // merged position of the k-th long tile / k-th short tile: order by the stamps
@@ -485,12 +498,12 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
             // plain (rank, row, m) order: the position among all tiles of this thread's range
             const int plain = run_l + run_s + m;
-            const int at = (seg_mode || !mix) ? plain
-                           : n > 2            ? pos_long(run_l + m)
-                                              : pos_short(run_s + m);
+            const int at = !mix            ? plain
+                           : is_long(n, l)   ? pos_long(run_l + m)
+                                             : pos_short(run_s + m);
             ws.tiles[at] = t;
         }
-        if (n > 2) run_l += n;
+        if (is_long(n, l)) run_l += n;
         else run_s += n;
     }
     if (threadIdx.x == 0) {
