@@ -19,9 +19,12 @@ Pieces:
 
 Parity status: every function is pinned by the ``-m "not gpu"`` tests
 (closed forms, brute force on tiny inputs, library routines for special
-cases) EXCEPT the choice made by the planning rule among valid plans, which
-the pages leave open ("near-optimal"): that choice is "parity unpinned"; its
-validity is pinned by ``check_plan`` and by brute force.
+cases, hand-worked examples). The pages leave the planner's choice among
+valid plans open ("near-optimal"); the oracle follows one documented rule (a
+reading of the pages), pinned to that rule by plans worked out by hand from
+its definition, and to validity by ``check_plan`` and by brute force over
+every parent function on small cases. Whether MoonEP's own planner makes the
+same choice cannot be decided from the pages.
 """
 from __future__ import annotations
 

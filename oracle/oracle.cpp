@@ -23,9 +23,11 @@
 // [E+B, H, H'] weight tensor, and reduce_grad (fold the replica gradients into
 // the home rows, zero the consumed slots). They do NOT state the planning
 // algorithm ("near-optimal"); this file implements one deterministic rule,
-// stated in plan_tree() below. Parity with MoonEP's own planner choice is
-// therefore unpinned; validity of a plan is pinned by oracle_check_plan(),
-// which is independent of the rule.
+// stated in plan_tree() below, a reading of the pages. The tests pin this
+// file's plans to that rule (plans worked out by hand from its definition);
+// whether MoonEP's own planner makes the same choice among valid plans cannot
+// be decided from the pages. Validity of a plan is pinned by
+// oracle_check_plan(), which is independent of the rule, and by brute force.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared (no FMA contraction,
 // so every fused multiply-add below is the explicit std::fma call). The same
