@@ -334,36 +334,64 @@ __global__ void __launch_bounds__(kSolveThreads) plan_solve_kernel(Dims d, Works
     if (tid == 0) ws.pfirst[E] = npieces;
     __syncthreads();
 
-    // 5. inference: top-B remote experts of each child get slots, the rest overflow
+    // 5. inference: top-B remote experts of each child get slots, the rest overflow.
+    //    One warp per child u of group g. A child's range is contiguous in g's list and
+    //    each expert's run is contiguous, so expert e has at most one piece on u. Each of
+    //    B rounds picks the unselected piece with the most slots, ties to the lower expert
+    //    id (a warp argmax over the lanes' own bests, each lane scanning its experts in
+    //    ascending id); then the selected experts take slots E+0.. in ascending id and the
+    //    others overflow onto their home rows.
     if (d.mode == BEP_INFER) {
-        for (int u = tid; u < R; u += nth) {
+        const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+        for (int u = warp; u < R; u += nwarps) {
             const int g = sParent[u];
             if (g < 0) continue;
-            // u's pieces are those of group g's experts with prank == u; their count is plen
-            for (int j = 0; j < B; ++j) {
-                int best = -1, bestlen = -1, bestidx = -1;
-                for (int e = g * G; e < (g + 1) * G; ++e)
-                    for (int i = ws.pfirst[e]; i < ws.pfirst[e + 1]; ++i)
-                        if (ws.prank[i] == u && ws.prow[i] == -1 && ws.plen[i] > bestlen) {
-                            best = e;
-                            bestlen = ws.plen[i];
-                            bestidx = i;
-                        }
-                if (best < 0) break;
-                ws.prow[bestidx] = -2;   // selected
-            }
-            int j = 0;
-            for (int e = g * G; e < (g + 1) * G; ++e)
+            auto piece_on_u = [&](int e) -> int {
                 for (int i = ws.pfirst[e]; i < ws.pfirst[e + 1]; ++i)
-                    if (ws.prank[i] == u) {
-                        if (ws.prow[i] == -2) {
-                            ws.prow[i] = E + j;
-                            slot_expert[u * B + j] = e;
-                            ++j;
-                        } else {
-                            ws.prow[i] = e;   // overflow: the GEMM reads home row e
-                        }
+                    if (ws.prank[i] == u) return i;
+                return -1;
+            };
+            for (int j = 0; j < B; ++j) {
+                int bl = -1, be = 0x7fffffff, bi = -1;
+                for (int e = g * G + lane; e < (g + 1) * G; e += 32) {
+                    const int i = piece_on_u(e);
+                    if (i >= 0 && ws.prow[i] == -1 && ws.plen[i] > bl) {
+                        bl = ws.plen[i];
+                        be = e;
+                        bi = i;
                     }
+                }
+                for (int o = 16; o > 0; o >>= 1) {
+                    const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (ol > bl || (ol == bl && oe < be)) {
+                        bl = ol;
+                        be = oe;
+                        bi = oi;
+                    }
+                }
+                if (bl < 0) break;          // the same on every lane
+                if (lane == 0) ws.prow[bi] = -2;   // selected
+                __syncwarp();
+            }
+            int jrun = 0;
+            for (int base = g * G; base < (g + 1) * G; base += 32) {
+                const int e = base + lane;
+                const int i = e < (g + 1) * G ? piece_on_u(e) : -1;
+                const bool sel = i >= 0 && ws.prow[i] == -2;
+                const unsigned m = __ballot_sync(0xffffffffu, sel);
+                if (i >= 0) {
+                    if (sel) {
+                        const int jj = jrun + __popc(m & ((1u << lane) - 1u));
+                        ws.prow[i] = E + jj;
+                        slot_expert[u * B + jj] = e;
+                    } else {
+                        ws.prow[i] = e;   // overflow: the GEMM reads home row e
+                    }
+                }
+                jrun += __popc(m);
+            }
         }
         __syncthreads();
     }
