@@ -72,8 +72,6 @@ __device__ __forceinline__ int load_dest(const int32_t* __restrict__ dest, int64
     return dl;
 }
 
-// ----------------------------------------------------------------------------- dispatch
-// recv[dest[tok, k], :] = x[tok, :]
 // The vectors [*v_lo, *v_hi) of item `item`'s row piece, for rows of nvec vectors cut
 // into `pieces` runs of whole 32*U-vector steps; returns the item's token.
 template <int U>
@@ -93,6 +91,8 @@ __device__ __forceinline__ int64_t piece_of(int64_t item, int pieces, int nvec, 
     return tok;
 }
 
+// ----------------------------------------------------------------------------- dispatch
+// recv[dest[tok, k], :] = x[tok, :]
 template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ dest,
