@@ -33,10 +33,11 @@ WORKLOAD = "bench_r8_e384"
 TARGETS = (0.2, 1.0, 10.0, 20.0)
 METRIC = "dispatch+combine tokens/s and HBM GB/s vs peak, maxvio 0.2-20, 1 GB300"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the forward
-# grouped GEMM, from one ncu capture of this bench at full size (mean over the four
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per forward grouped GEMM call
+# (its two launches: the segments of 2,048 rows or more with two m-tiles per unit, then
+# the others), from one ncu capture of this bench at full size (mean over the four
 # routings). Must be reset to None whenever that kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 23.51e9}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"bench_r8_e384": 23.84e9}
 
 # Input sets the end-to-end loop keeps on the device: uploads run up to this many steps
 # ahead of compute (1.5 GB per set at the S=8192, E=384 workload, 18 GB in all).
@@ -792,7 +793,11 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": traffic},
         "e2e": {"value": world * tokens_per_step * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 12 * args.steps,
+        # our kernels per step: plan 4, prefetch 1, dispatch 1, GEMM 2 (work list, GEMM) or 4
+        # (the library's two-launch forward: H >= 2048, 256 | H', at least 512 receive rows
+        # per expert), combine 1, combine backward 1, reduce_grad 2
+        "gpu_launches": (12 + (2 if (H >= 2048 and Hp % 256 == 0 and R * S * K >= 512 * E) else 0))
+                        * args.steps,
         "clocks": clocks,
         "backward": bwd,
         "prefetch_overlap": overlap,

@@ -54,15 +54,18 @@ constexpr int kOutBox = 32 * 128;               // epilogue staging box: 32 rows
                                                 // (DW: 32 fp32 columns; FWD/DX: 64 bf16 columns)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2 };
+// kFwd2: the forward product with a unit of two 128-row m-tiles of one segment that
+// share each weight stage (two accumulators, one per m-tile).
+enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2, kFwd2 = 3 };
 
 template <int MODE>
 struct ModeCfg {
     static constexpr bool kAmn = MODE == kDw;          // A operand MN-major (recv^T)
     static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
-    static constexpr int kEpiWarps = MODE == kDw ? 8 : 4;
-    static constexpr int kStages = 4;
-    static constexpr int kOutBufs = MODE == kDw ? 1 : 2;   // staging boxes per epilogue warp
+    static constexpr int kEpiWarps = (MODE == kDw || MODE == kFwd2) ? 8 : 4;
+    static constexpr int kStages = MODE == kFwd2 ? 3 : 4;
+    static constexpr int kOutBufs = (MODE == kDw || MODE == kFwd2) ? 1 : 2;   // staging boxes per epilogue warp
+    static constexpr int kATiles = MODE == kFwd2 ? 2 : 1;  // A tiles (128 rows) per stage
     static constexpr int kWarps = 2 + kEpiWarps;
     static constexpr int kThreads = 32 * kWarps;
 };
@@ -410,6 +413,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   segment's tiles keep their order, with at most a few short tiles between two
 //   of them. Otherwise (training sizes: a few short segments among many long ones)
 //   the order is plain (rank, row, m).
+// seg_mode == 3: as 0 with tiles of <= 256 rows (two m-tiles: the kFwd2 units), for the
+//   segments of kDualMinRows rows or more only; seg_mode == 4: as 0 for the other segments.
 // seg_mode == 1: one entry per non-empty segment, rows = its length (DW).
 // seg_mode == 2: as 1, plus an entry with rows = 0 for every expert whose home segment
 //   (rank e / (E/R), row e) is empty, so that an overwriting DW writes its zeros; a
@@ -421,9 +426,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   segments hold fewer than 256 rows); merged evenly, CTAs on short segments move
 //   gradients while the others keep the tensor pipes busy.
 constexpr int kDwShortRows = 1024;
+constexpr int kDualMinRows = 2048;
 
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
+    const bool dw = seg_mode == 1 || seg_mode == 2;
+    // FWD/DX: rows per tile (kFwd2: two m-tiles)
+    const int tile = seg_mode == 3 ? 2 * kBM : kBM;
+    auto tile_of = [&](int) { return tile; };
     __shared__ int s_warp[33];
     const int n_items = d.R * d.NROW;
     const int per = (n_items + blockDim.x - 1) / blockDim.x;
@@ -445,11 +455,15 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
             if (b > a) bad = 1;
             return 0;
         }
-        if (seg_mode) return b > a ? 1 : 0;
-        return (b - a + kBM - 1) / kBM;
+        if (dw) return b > a ? 1 : 0;
+        // seg_mode 3 takes the segments of kDualMinRows rows or more, seg_mode 4 the others
+        if ((seg_mode == 3 && b - a < kDualMinRows) || (seg_mode == 4 && b - a >= kDualMinRows))
+            return 0;
+        const int tl = tile_of(b - a);
+        return (b - a + tl - 1) / tl;
     };
     // FWD/DX: a segment of three or more m-tiles is long; DW: one of kDwShortRows rows or more
-    auto is_long = [&](int n, int l) { return seg_mode ? l >= kDwShortRows : n > 2; };
+    auto is_long = [&](int n, int l) { return dw ? l >= kDwShortRows : l > 2 * kBM; };
     // the merge is for the accumulating DW only: the overwriting one reads no gradient, its
     // short segments' units are light, and there merging measured no faster
     int nlong = 0, nshort = 0;
@@ -492,8 +506,9 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
         const int wsel = rho < d.E ? rho : -(1 + u * d.B + (rho - d.E));
         for (int m = 0; m < n; ++m) {
             MTile t;
-            t.row0 = (int32_t)(u * d.C + s + m * kBM);
-            t.rows = seg_mode ? l : min(kBM, l - m * kBM);
+            const int tl = tile_of(l);
+            t.row0 = (int32_t)(u * d.C + s + m * tl);
+            t.rows = dw ? l : min(tl, l - m * tl);
             t.wsel = wsel;
             t.pad = u * d.NROW + rho;   // row of rank u's [E+B] view
             // plain (rank, row, m) order: the position among all tiles of this thread's range
@@ -576,7 +591,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
     const int b_bytes = BN * kBK * 2;
     uint8_t* smA = smem;
     constexpr int kStages = CF::kStages;
-    uint8_t* smB = smem + kStages * kABytes;
+    constexpr int kAStage = CF::kATiles * kABytes;   // A bytes per stage
+    uint8_t* smB = smem + kStages * kAStage;
     uint8_t* smO = smB + kStages * b_bytes;   // a 4 KB staging box per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smO + CF::kEpiWarps * CF::kOutBufs * kOutBox);
     uint64_t* full = bars;
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 
     const int NT = p.N / BN;
     const int total = MODE == kDw ? *p.ntiles * p.mtd * NT : *p.ntiles * NT;
-    const uint32_t stage_bytes = (uint32_t)(kABytes + b_bytes);
+    const uint32_t stage_bytes = (uint32_t)(kAStage + b_bytes);
     const int acc_stride = p.tmem_cols / 2;   // two accumulators, power-of-two spaced columns
     uint32_t pr_s = 0, pr_ph = 0, pr_armed = 0;   // the producer's ring position and stages armed
 
@@ -630,8 +646,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 const int n0 = u.nt * BN;
                 const CUtensorMap* tmB = (MODE == kDw || p.vm || u.t.wsel >= 0) ? &tmB0 : &tmB1;
                 const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
-                if (MODE == kFwd) {
+                if (MODE == kFwd || MODE == kFwd2) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
+                    if (MODE == kFwd2 && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
                     for (int c = 0; c < BN / 64; ++c) op(tmB, 2 + c, n0 + c * 64, brow0 + kb * kBK);
                 } else if (MODE == kDx) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
@@ -655,18 +672,21 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             int it = 0;
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
-                const bool rev = MODE == kFwd && (it & 1);
+                const bool rev = (MODE == kFwd || MODE == kFwd2) && (it & 1);
+                const uint32_t ubytes =
+                    (MODE == kFwd2 && u.t.rows <= kBM) ? stage_bytes - (uint32_t)kABytes : stage_bytes;
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    mbar_arrive_expect_tx(&full[s], ubytes);
                     ++pr_armed;
-                    uint8_t* a_dst = smA + s * kABytes;
+                    uint8_t* a_dst = smA + s * kAStage;
                     uint8_t* b_dst = smB + s * b_bytes;
                     kblock(u, rev ? u.kb_n - 1 - kb : kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
-                        uint8_t* dst = piece < 2 ? a_dst + piece * kBChunkBytes
+                        // A: DW's two 8 KB column chunks, or kFwd2's second 128-row tile
+                        uint8_t* dst = piece < 2 ? a_dst + piece * (MODE == kFwd2 ? kABytes : kBChunkBytes)
                                                  : b_dst + (piece - 2) * kBChunkBytes;
                         tma_load_2d(m, &full[s], dst, c0, c1);
                     });
@@ -694,12 +714,67 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
             const Unit u = unit_at<MODE>(p, unit, NT);
             const uint32_t idesc = (MODE != kDw && u.t.rows <= kBM / 2) ? idesc_half : idesc_full;
-            const int acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            // kFwd2: both accumulators belong to one unit (m-tile 0 in the first, m-tile 1,
+            // if the unit has one, in the second), so units alternate on one barrier pair
+            const int acc = MODE == kFwd2 ? 0 : it & 1;
+            const uint32_t aph = MODE == kFwd2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+            const bool two = MODE == kFwd2 && u.t.rows > kBM;
+            const uint32_t idesc1 = (u.t.rows - kBM <= kBM / 2) ? idesc_half : idesc_full;
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
             tc_fence_after();
             const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
-            for (int kb = 0; kb < u.kb_n; ++kb) {
+            const uint32_t dt1 = tmem_base + (uint32_t)acc_stride;
+            int kb = 0;
+            if (MODE == kFwd2 && two) {
+                // The epilogue frees the first accumulator before it drains the second:
+                // run the first m-tile's MMAs over the stages already in the ring (up to all
+                // of them) while the second accumulator is drained, then the second m-tile's
+                // on the same stages, and only then release those stages. A unit of one
+                // m-tile needs only the first accumulator and takes the plain loop.
+                const int pre = min(kStages, u.kb_n);
+                uint32_t s0 = s, ph0 = ph;
+                for (int j = 0; j < pre && live; ++j) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s0], ph0, s_abort, status))) {
+                        live = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(smA + s0 * kAStage);
+                        const uint32_t b0 = smem_u32(smB + s0 * b_bytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
+                                     idesc, (j | kk) != 0);
+                    }
+                    __syncwarp();
+                    if (++s0 == kStages) {
+                        s0 = 0;
+                        ph0 ^= 1u;
+                    }
+                }
+                if (!live) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&tempty[1], aph ^ 1u, s_abort, status))) break;
+                tc_fence_after();
+                for (int j = 0; j < pre; ++j) {
+                    if (lane == 0) {
+                        const uint32_t a1 = smem_u32(smA + s * kAStage) + kABytes;
+                        const uint32_t b0 = smem_u32(smB + s * b_bytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(dt1, operand_desc<CF::kAmn>(a1, kk), operand_desc<CF::kBmn>(b0, kk),
+                                     idesc1, (j | kk) != 0);
+                        mma_commit(&empty[s]);
+                    }
+                    __syncwarp();
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                kb = pre;
+            }
+            for (; kb < u.kb_n; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, s_abort, status))) {
                     live = false;
                     break;
@@ -725,13 +800,17 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 }
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smA + s * kABytes);
+                    const uint32_t a0 = smem_u32(smA + s * kAStage);
                     const uint32_t b0 = smem_u32(smB + s * b_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        if (kk < ksteps)
+                        if (kk < ksteps) {
                             mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
                                      idesc, (kb | kk) != 0);
+                            if (two)
+                                mma_bf16(dt1, operand_desc<CF::kAmn>(a0 + kABytes, kk),
+                                         operand_desc<CF::kBmn>(b0, kk), idesc1, (kb | kk) != 0);
+                        }
                     mma_commit(&empty[s]);
                 }
                 __syncwarp();
@@ -752,8 +831,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         int it = 0;
         int obox = 0, last_store = -1;   // FWD/DX: next staging box; box of the newest TMA store
         for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const int acc = MODE == kFwd2 ? 0 : it & 1;
+            const uint32_t aph = MODE == kFwd2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
             const bool got = mbar_wait(&tfull[acc], aph, s_abort, status);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
@@ -804,14 +883,19 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 // belong to the next segment's tile. Two boxes per warp alternate, so one
                 // store can be in flight while the next box is filled.
                 // this warp's rows: 32q..32q+31 of a full tile, or, of an M=64 tile,
-                // 16q..16q+15 in lanes 0-15 of its quadrant
-                const int wrows = u.t.rows <= kBM / 2 ? 16 : 32;
-                const int nvalid = min(wrows, u.t.rows - q * wrows);   // of them inside the segment
+                // 16q..16q+15 in lanes 0-15 of its quadrant; kFwd2 drains the unit's first
+                // m-tile from the first accumulator, then its second from the second
+                for (int half = 0; half < (MODE == kFwd2 ? 2 : 1); ++half) {
+                const int trows = MODE == kFwd2 ? min(u.t.rows - half * kBM, kBM) : u.t.rows;
+                const int trow0 = u.t.row0 + half * kBM;
+                const uint32_t tb = tbase + (uint32_t)(half * acc_stride);
+                const int wrows = trows <= kBM / 2 ? 16 : 32;
+                const int nvalid = min(wrows, trows - q * wrows);   // of them inside the segment
                 const int rsub = lane >> 3, piece = lane & 7;
-                const int orow = u.t.row0 + q * wrows;
+                const int orow = trow0 + q * wrows;
                 uint16_t* ybase = p.out + (int64_t)orow * p.N + (int64_t)u.nt * BN;
                 for (int c0 = c_lo; c0 < c_lo + cspan && nvalid > 0; c0 += 64) {
-                    const int b = obox++ & 1;
+                    const int b = obox++ % CF::kOutBufs;
                     uint8_t* stg = smO + (e * CF::kOutBufs + b) * kOutBox;
                     uint4* srow = reinterpret_cast<uint4*>(stg + lane * 128);
                     // a store issued from this box earlier has read it: every bulk group but the
@@ -825,7 +909,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + (uint32_t)(c0 + 32 * h), r);
+                        tmem_ld_32x32b_x32(tb + (uint32_t)(c0 + 32 * h), r);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 o;
@@ -857,10 +941,18 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                         __syncwarp();   // the box is read back before it is filled again
                     }
                 }
+                if (MODE == kFwd2) {   // this half's accumulator is free for the next unit
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[half]);
+                }
+                }   // half
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (MODE != kFwd2) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
         }
         // every store or reduce this warp issued has completed before the CTA ends
         if (lane == 0) bulk_wait_all();
@@ -1294,8 +1386,20 @@ template <int MODE>
 size_t smem_bytes(int BN) {
     using CF = ModeCfg<MODE>;
     const size_t stage_out = (size_t)CF::kEpiWarps * CF::kOutBufs * kOutBox;
-    return 1024 + (size_t)CF::kStages * (kABytes + BN * kBK * 2) + stage_out +
+    return 1024 + (size_t)CF::kStages * (CF::kATiles * kABytes + BN * kBK * 2) + stage_out +
            (2 * CF::kStages + 4) * 8 + 16;
+}
+
+// The forward runs the segments of kDualMinRows rows or more with two m-tiles per unit
+// (kFwd2: one weight stage feeds two 128-row m-tiles, both accumulators of TMEM, so
+// BN = 256), in a launch of its own before the other segments, when the batch has on
+// average at least kDualRows receive rows per expert and K is at least kDualMinK:
+// elsewhere (inference batches, small K) the two launches and the per-unit hand-over
+// between the two accumulators cost more than the halved weight reads save.
+constexpr int kDualRows = 512;
+constexpr int kDualMinK = 2048;
+bool use_dual(const Dims& d, int K, int BN) {
+    return BN == 256 && K >= kDualMinK && (int64_t)d.R * d.C >= (int64_t)kDualRows * d.E;
 }
 
 int tmem_cols_for(int BN) {
@@ -1349,6 +1453,9 @@ cudaError_t gemm_setup(int device) {
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_bytes<kFwd>(256));
     if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<kFwd2>(256));
+    if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_bytes<kDx>(256));
     if (err != cudaSuccess) return err;
@@ -1380,8 +1487,8 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     if (d.C == 0) return cudaSuccess;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
     const int BN = pick_bn(d.Hp);
+    const bool dual = use_dual(d, d.H, BN);
     CUtensorMap tmA, tmBh, tmBs;
     if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBM, kBK)) return cudaErrorInvalidValue;
     if (!encode_2d(&tmBh, w_home, (uint64_t)d.E * d.H, d.Hp, kBK, 64)) return cudaErrorInvalidValue;
@@ -1398,9 +1505,18 @@ cudaError_t launch_grouped_gemm(const Dims& d, const Workspace& ws, const int32_
     prm.Kdim = d.H;
     prm.H = d.H;
     prm.BN = BN;
-    prm.tmem_cols = tmem_cols_for(BN);
+    prm.tmem_cols = tmem_cols_for(BN);   // two BN-column accumulators (kFwd2: one unit's two)
     prm.mtd = 1;
     prm.status = ws.status;
+    if (!dual) {
+        gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
+        return launch_mode<kFwd>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
+    }
+    // long segments two m-tiles per unit, then the others one per unit
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 3);
+    err = launch_mode<kFwd2>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 4);
     return launch_mode<kFwd>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
 }
 
@@ -1414,8 +1530,8 @@ cudaError_t launch_grouped_gemm_vm(const Dims& d, const Workspace& ws, const int
     if (d.C == 0) return cudaSuccess;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
     const int BN = pick_bn(d.Hp);
+    const bool dual = use_dual(d, d.H, BN);
     CUtensorMap tmA, tmV;
     if (!encode_2d(&tmA, recv, (uint64_t)d.R * d.C, d.H, kBM, kBK)) return cudaErrorInvalidValue;
     if (!encode_2d(&tmV, w_views, (uint64_t)d.R * d.NROW * d.H, d.Hp, kBK, 64))
@@ -1428,12 +1544,20 @@ cudaError_t launch_grouped_gemm_vm(const Dims& d, const Workspace& ws, const int
     prm.Kdim = d.H;
     prm.H = d.H;
     prm.BN = BN;
-    prm.tmem_cols = tmem_cols_for(BN);
+    prm.tmem_cols = tmem_cols_for(BN);   // two BN-column accumulators (kFwd2: one unit's two)
     prm.mtd = 1;
     prm.vm = 1;
     prm.status = ws.status;
     CUtensorMap tmY;
     if (!encode_2d(&tmY, y, (uint64_t)d.R * d.C, d.Hp, 32, 64)) return cudaErrorInvalidValue;
+    if (!dual) {
+        gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
+        return launch_mode<kFwd>(tmA, tmV, tmV, tmY, tmY, prm, num_sms, st);
+    }
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 3);
+    err = launch_mode<kFwd2>(tmA, tmV, tmV, tmY, tmY, prm, num_sms, st);
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 4);
     return launch_mode<kFwd>(tmA, tmV, tmV, tmY, tmY, prm, num_sms, st);
 }
 

@@ -1,0 +1,133 @@
+"""The forward GEMM's two-m-tile units, on hand-made cu_seqlens tables.
+
+Segments of 2,048 rows or more run in a launch of their own with two 128-row
+m-tiles per unit sharing each weight stage (the second m-tile of a unit may be
+ragged, down to one row, or absent), the other segments in the usual one-m-tile
+launch. These tables mix both kinds with every tail case: an even number of
+m-tiles, an odd number (the last unit holds one m-tile), a second m-tile of at
+most 64 rows (M=64 MMAs), a first m-tile of at most 64 rows, and short
+segments. Compared with the binary64 oracle in full (relative Frobenius per
+segment and every element against the fp32-accumulation bound), exactly with
+permutation weights, rows outside every segment untouched, and the
+two-pointer GEMM equal bit for bit to the VM GEMM on materialised views."""
+import numpy as np
+import pytest
+import torch
+
+import elementwise as ew
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+RTOL = 2e-2
+
+# R=2, E=4 (2 home experts per rank), B=2, K=2, S=4096: C=8192 rows per rank.
+# H=2048 (the reduction length) and H'=256 (one 256-column tile): the conditions
+# under which the two-m-tile launch runs.
+R, E, B, K, S, H, HP = 2, 4, 2, 2, 4096, 2048, 256
+C = S * K
+LENGTHS = [
+    [2048, 2177, 1500, 2100, 300, 64],      # 16 m-tiles; 1-row second tile; short; 52-row unit
+    [2113, 2276, 0, 1, 1752, 2050],         # 65-row one-tile unit; 100-row second tile; 1; 2-row unit
+]
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(DEV).view(
+        torch.bfloat16)
+
+
+def host_u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def nz(a):
+    """bf16 bit patterns with -0 written as +0: a sum of signed zeros may carry either sign."""
+    a = np.array(a, np.uint16)
+    a[a == 0x8000] = 0
+    return a
+
+
+def table():
+    cu = np.zeros((R, E + B + 1), np.int32)
+    for u in range(R):
+        cu[u, 1:] = np.cumsum(LENGTHS[u])
+    assert cu[:, -1].max() <= C
+    return cu
+
+
+def covered(cu):
+    m = np.zeros(R * C, bool)
+    for u in range(R):
+        m[u * C:u * C + int(cu[u, -1])] = True
+    return m
+
+
+def test_lengths_reach_both_launches():
+    assert table()[:, -1].max() <= C
+    flat = [n for row in LENGTHS for n in row if n > 0]
+    assert any(n >= 2048 and (n + 127) // 128 % 2 == 0 for n in flat)     # even m-tile count
+    assert any(n >= 2048 and (n + 127) // 128 % 2 == 1 for n in flat)     # odd: a one-m-tile unit
+    assert any(n >= 2048 and 0 < n % 256 - 128 <= 64 for n in flat)       # second m-tile <= 64 rows
+    assert any(n >= 2048 and 0 < n % 256 <= 64 for n in flat)             # first m-tile <= 64 rows
+    assert any(0 < n < 2048 for n in flat)                                # the one-m-tile launch
+
+
+def test_forward_two_mtile_units_against_binary64(lib):
+    bep = lib
+    ctx = bep.Context(bep.Config(R, E, B, K, S, H, HP, 0))
+    cu = table()
+    recv = synth.tokens_host((R * C, H), 701)
+    w_home = synth.weights_host((E, H, HP), 702)
+    w_slots = synth.weights_host((R, B, H, HP), 703)
+    y = torch.full((R * C, HP), -5.0, dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm(ctx, torch.from_numpy(cu).to(DEV), dev_u16(recv), dev_u16(w_home),
+                         dev_u16(w_slots), y)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    ref = oracle.grouped_gemm(recv, w_home, w_slots, cu, E)
+    got = oracle.bf16_to_f32(host_u16(y)).astype(np.float64)
+    for u, rho, a, b in ew.segments(cu, E, C):
+        err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
+        assert err <= RTOL, (u, rho, b - a, err)
+    wh = oracle.bf16_to_f32(w_home).astype(np.float64)
+    ws = oracle.bf16_to_f32(w_slots).astype(np.float64)
+    worst = ew.gemm_table("fwd", got, ref, oracle.bf16_to_f32(recv).astype(np.float64), cu, E, C,
+                          lambda u, rho: wh[rho] if rho < E else ws[u, rho - E])
+    assert (got[~covered(cu)] == -5.0).all()
+    print(f"two-m-tile forward: {worst}")
+
+
+def test_forward_two_mtile_units_exact_and_equal_to_vm(lib):
+    """Permutation weights (one 1.0 per column, a shift per weight row): every output
+    is one input element, so a wrong m-tile, accumulator, row or weight row shows."""
+    bep = lib
+    ctx = bep.Context(bep.Config(R, E, B, K, S, H, HP, 0))
+    cu = table()
+    cu_d = torch.from_numpy(cu).to(DEV)
+    recv = synth.tokens_host((R * C, H), 711)
+
+    def perm(shift):
+        w = np.zeros((H, HP), np.float32)
+        w[(np.arange(HP) + shift) % H, np.arange(HP)] = 1.0
+        return oracle.f32_to_bf16(w)
+    w_home = np.stack([perm(37 * e + 5) for e in range(E)])
+    w_slots = np.stack([np.stack([perm(37 * (E + u * B + j) + 5) for j in range(B)]) for u in range(R)])
+    y = torch.zeros((R * C, HP), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm(ctx, cu_d, dev_u16(recv), dev_u16(w_home), dev_u16(w_slots), y)
+    # the same weights as R materialised [E+B, H, H'] views, through the VM GEMM
+    views = np.concatenate([np.concatenate([w_home, w_slots[u]], axis=0)[None] for u in range(R)])
+    y_vm = torch.zeros_like(y)
+    bep.bep_grouped_gemm_vm(ctx, cu_d, dev_u16(recv), dev_u16(views), y_vm)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    want = oracle.f32_to_bf16(oracle.grouped_gemm(recv, w_home, w_slots, cu, E).astype(np.float32))
+    got = host_u16(y)
+    for u, rho, a, b in ew.segments(cu, E, C):
+        shift = 37 * (rho if rho < E else E + u * B + (rho - E)) + 5
+        cols = (np.arange(HP) + shift) % H
+        np.testing.assert_array_equal(nz(want[a:b]), nz(recv[a:b][:, cols]))
+    np.testing.assert_array_equal(nz(got), nz(want))
+    assert torch.equal(y.view(torch.int16), y_vm.view(torch.int16))
