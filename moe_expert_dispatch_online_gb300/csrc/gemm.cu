@@ -54,18 +54,19 @@ constexpr int kOutBox = 32 * 128;               // epilogue staging box: 32 rows
                                                 // (DW: 32 fp32 columns; FWD/DX: 64 bf16 columns)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-// kFwd2: the forward product with a unit of two 128-row m-tiles of one segment that
-// share each weight stage (two accumulators, one per m-tile).
-enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2, kFwd2 = 3 };
+// kFwd2 / kDx2: the forward / input-gradient product with a unit of two 128-row m-tiles
+// of one segment that share each weight stage (two accumulators, one per m-tile).
+enum GemmMode : int { kFwd = 0, kDx = 1, kDw = 2, kFwd2 = 3, kDx2 = 4 };
 
 template <int MODE>
 struct ModeCfg {
+    static constexpr bool kDual = MODE == kFwd2 || MODE == kDx2;   // two m-tiles per unit
     static constexpr bool kAmn = MODE == kDw;          // A operand MN-major (recv^T)
-    static constexpr bool kBmn = MODE != kDx;          // B operand MN-major
-    static constexpr int kEpiWarps = (MODE == kDw || MODE == kFwd2) ? 8 : 4;
-    static constexpr int kStages = MODE == kFwd2 ? 3 : 4;
-    static constexpr int kOutBufs = (MODE == kDw || MODE == kFwd2) ? 1 : 2;   // staging boxes per epilogue warp
-    static constexpr int kATiles = MODE == kFwd2 ? 2 : 1;  // A tiles (128 rows) per stage
+    static constexpr bool kBmn = MODE != kDx && MODE != kDx2;   // B operand MN-major
+    static constexpr int kEpiWarps = (MODE == kDw || kDual) ? 8 : 4;
+    static constexpr int kStages = kDual ? 3 : 4;
+    static constexpr int kOutBufs = (MODE == kDw || kDual) ? 1 : 2;   // staging boxes per epilogue warp
+    static constexpr int kATiles = kDual ? 2 : 1;  // A tiles (128 rows) per stage
     static constexpr int kWarps = 2 + kEpiWarps;
     static constexpr int kThreads = 32 * kWarps;
 };
@@ -648,10 +649,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
                 if (MODE == kFwd || MODE == kFwd2) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
-                    if (MODE == kFwd2 && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
+                    if (CF::kDual && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
                     for (int c = 0; c < BN / 64; ++c) op(tmB, 2 + c, n0 + c * 64, brow0 + kb * kBK);
-                } else if (MODE == kDx) {
+                } else if (MODE == kDx || MODE == kDx2) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
+                    if (CF::kDual && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
                     op(tmB, 2, kb * kBK, brow0 + n0);
                 } else {
                     const int r0 = u.t.row0 + kb * kBK;
@@ -674,7 +676,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 const Unit u = unit_at<MODE>(p, unit, NT);
                 const bool rev = (MODE == kFwd || MODE == kFwd2) && (it & 1);
                 const uint32_t ubytes =
-                    (MODE == kFwd2 && u.t.rows <= kBM) ? stage_bytes - (uint32_t)kABytes : stage_bytes;
+                    (CF::kDual && u.t.rows <= kBM) ? stage_bytes - (uint32_t)kABytes : stage_bytes;
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
@@ -685,8 +687,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                     uint8_t* a_dst = smA + s * kAStage;
                     uint8_t* b_dst = smB + s * b_bytes;
                     kblock(u, rev ? u.kb_n - 1 - kb : kb, [&](const CUtensorMap* m, int piece, int c0, int c1) {
-                        // A: DW's two 8 KB column chunks, or kFwd2's second 128-row tile
-                        uint8_t* dst = piece < 2 ? a_dst + piece * (MODE == kFwd2 ? kABytes : kBChunkBytes)
+                        // A: DW's two 8 KB column chunks, or a dual unit's second 128-row tile
+                        uint8_t* dst = piece < 2 ? a_dst + piece * (CF::kDual ? kABytes : kBChunkBytes)
                                                  : b_dst + (piece - 2) * kBChunkBytes;
                         tma_load_2d(m, &full[s], dst, c0, c1);
                     });
@@ -714,18 +716,18 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
             const Unit u = unit_at<MODE>(p, unit, NT);
             const uint32_t idesc = (MODE != kDw && u.t.rows <= kBM / 2) ? idesc_half : idesc_full;
-            // kFwd2: both accumulators belong to one unit (m-tile 0 in the first, m-tile 1,
-            // if the unit has one, in the second), so units alternate on one barrier pair
-            const int acc = MODE == kFwd2 ? 0 : it & 1;
-            const uint32_t aph = MODE == kFwd2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
-            const bool two = MODE == kFwd2 && u.t.rows > kBM;
+            // dual modes: both accumulators belong to one unit (m-tile 0 in the first, m-tile
+            // 1, if the unit has one, in the second), so units alternate on one barrier pair
+            const int acc = CF::kDual ? 0 : it & 1;
+            const uint32_t aph = CF::kDual ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+            const bool two = CF::kDual && u.t.rows > kBM;
             const uint32_t idesc1 = (u.t.rows - kBM <= kBM / 2) ? idesc_half : idesc_full;
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
             tc_fence_after();
             const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
             const uint32_t dt1 = tmem_base + (uint32_t)acc_stride;
             int kb = 0;
-            if (MODE == kFwd2 && two) {
+            if (CF::kDual && two) {
                 // The epilogue frees the first accumulator before it drains the second:
                 // run the first m-tile's MMAs over the stages already in the ring (up to all
                 // of them) while the second accumulator is drained, then the second m-tile's
@@ -831,8 +833,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         int it = 0;
         int obox = 0, last_store = -1;   // FWD/DX: next staging box; box of the newest TMA store
         for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
-            const int acc = MODE == kFwd2 ? 0 : it & 1;
-            const uint32_t aph = MODE == kFwd2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+            const int acc = CF::kDual ? 0 : it & 1;
+            const uint32_t aph = CF::kDual ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
             const bool got = mbar_wait(&tfull[acc], aph, s_abort, status);
             __syncwarp();
             if (!__all_sync(0xffffffffu, got)) break;
@@ -883,10 +885,10 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 // belong to the next segment's tile. Two boxes per warp alternate, so one
                 // store can be in flight while the next box is filled.
                 // this warp's rows: 32q..32q+31 of a full tile, or, of an M=64 tile,
-                // 16q..16q+15 in lanes 0-15 of its quadrant; kFwd2 drains the unit's first
+                // 16q..16q+15 in lanes 0-15 of its quadrant; a dual unit drains its first
                 // m-tile from the first accumulator, then its second from the second
-                for (int half = 0; half < (MODE == kFwd2 ? 2 : 1); ++half) {
-                const int trows = MODE == kFwd2 ? min(u.t.rows - half * kBM, kBM) : u.t.rows;
+                for (int half = 0; half < (CF::kDual ? 2 : 1); ++half) {
+                const int trows = CF::kDual ? min(u.t.rows - half * kBM, kBM) : u.t.rows;
                 const int trow0 = u.t.row0 + half * kBM;
                 const uint32_t tb = tbase + (uint32_t)(half * acc_stride);
                 const int wrows = trows <= kBM / 2 ? 16 : 32;
@@ -941,14 +943,14 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                         __syncwarp();   // the box is read back before it is filled again
                     }
                 }
-                if (MODE == kFwd2) {   // this half's accumulator is free for the next unit
+                if (CF::kDual) {   // this half's accumulator is free for the next unit
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[half]);
                 }
                 }   // half
             }
-            if (MODE != kFwd2) {
+            if (!CF::kDual) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -1456,6 +1458,9 @@ cudaError_t gemm_setup(int device) {
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kFwd2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_bytes<kFwd2>(256));
     if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<kDx2>(256));
+    if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(grouped_gemm_kernel<kDx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_bytes<kDx>(256));
     if (err != cudaSuccess) return err;
@@ -1568,8 +1573,8 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
     if (d.C == 0) return cudaSuccess;
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
-    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
     const int BN = pick_bn(d.H);
+    const bool dual = use_dual(d, d.Hp, BN);
     CUtensorMap tmA, tmBh, tmBs;
     // A: dY [R*C, H'] rows, 64-wide K boxes; B: W rows h (N) x 64 columns h' (K)
     if (!encode_2d(&tmA, dy, (uint64_t)d.R * d.C, d.Hp, kBM, kBK)) return cudaErrorInvalidValue;
@@ -1587,9 +1592,18 @@ cudaError_t launch_grouped_gemm_dx(const Dims& d, const Workspace& ws, const int
     prm.Kdim = d.Hp;
     prm.H = d.H;
     prm.BN = BN;
-    prm.tmem_cols = tmem_cols_for(BN);
+    prm.tmem_cols = tmem_cols_for(BN);   // two BN-column accumulators (kDx2: one unit's two)
     prm.mtd = 1;
     prm.status = ws.status;
+    if (!dual) {
+        gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 0);
+        return launch_mode<kDx>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
+    }
+    // as the forward: long segments two m-tiles per unit, then the others one per unit
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 3);
+    err = launch_mode<kDx2>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
+    if (err != cudaSuccess) return err;
+    gemm_tiles_kernel<<<1, 1024, 0, st>>>(cu, d, ws, 4);
     return launch_mode<kDx>(tmA, tmBh, tmBs, tmY, tmY, prm, num_sms, st);
 }
 

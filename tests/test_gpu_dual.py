@@ -9,7 +9,8 @@ most 64 rows (M=64 MMAs), a first m-tile of at most 64 rows, and short
 segments. Compared with the binary64 oracle in full (relative Frobenius per
 segment and every element against the fp32-accumulation bound), exactly with
 permutation weights, rows outside every segment untouched, and the
-two-pointer GEMM equal bit for bit to the VM GEMM on materialised views."""
+two-pointer GEMM equal bit for bit to the VM GEMM on materialised views. The
+input-gradient GEMM takes the same two launches and is checked the same way."""
 import numpy as np
 import pytest
 import torch
@@ -131,3 +132,60 @@ def test_forward_two_mtile_units_exact_and_equal_to_vm(lib):
         np.testing.assert_array_equal(nz(want[a:b]), nz(recv[a:b][:, cols]))
     np.testing.assert_array_equal(nz(got), nz(want))
     assert torch.equal(y.view(torch.int16), y_vm.view(torch.int16))
+
+
+# The input gradient dRecv = dY W^T runs the same two launches when H (its N) is a multiple
+# of 256 and H' (its reduction length) is at least 2048: H=256, H'=2048 on the same tables.
+H_DX, HP_DX = 256, 2048
+
+
+def test_input_gradient_two_mtile_units_against_binary64(lib):
+    bep = lib
+    ctx = bep.Context(bep.Config(R, E, B, K, S, H_DX, HP_DX, 0))
+    cu = table()
+    dy = synth.tokens_host((R * C, HP_DX), 721)
+    w_home = synth.weights_host((E, H_DX, HP_DX), 722)
+    w_slots = synth.weights_host((R, B, H_DX, HP_DX), 723)
+    drecv = torch.full((R * C, H_DX), 3.0, dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, torch.from_numpy(cu).to(DEV), dev_u16(dy), dev_u16(w_home),
+                            dev_u16(w_slots), drecv)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    ref = oracle.grouped_gemm_dx(dy, w_home, w_slots, cu, E)
+    got = oracle.bf16_to_f32(host_u16(drecv)).astype(np.float64)
+    for u, rho, a, b in ew.segments(cu, E, C):
+        err = np.linalg.norm(got[a:b] - ref[a:b]) / max(np.linalg.norm(ref[a:b]), 1e-30)
+        assert err <= RTOL, (u, rho, b - a, err)
+    wh = oracle.bf16_to_f32(w_home).astype(np.float64)
+    ws = oracle.bf16_to_f32(w_slots).astype(np.float64)
+    worst = ew.gemm_table("dx", got, ref, oracle.bf16_to_f32(dy).astype(np.float64), cu, E, C,
+                          lambda u, rho: wh[rho] if rho < E else ws[u, rho - E])
+    assert (got[~covered(cu)] == 3.0).all()
+    print(f"two-m-tile input gradient: {worst}")
+
+
+def test_input_gradient_two_mtile_units_exact(lib):
+    """One 1.0 per weight row h, at column sigma(h) = (8h + shift) mod H' (distinct per h):
+    every dRecv[row, h] is the single element dY[row, sigma(h)]."""
+    bep = lib
+    ctx = bep.Context(bep.Config(R, E, B, K, S, H_DX, HP_DX, 0))
+    cu = table()
+    dy = synth.tokens_host((R * C, HP_DX), 731)
+
+    def perm(shift):
+        w = np.zeros((H_DX, HP_DX), np.float32)
+        w[np.arange(H_DX), (8 * np.arange(H_DX) + shift) % HP_DX] = 1.0
+        return oracle.f32_to_bf16(w)
+    w_home = np.stack([perm(41 * e + 3) for e in range(E)])
+    w_slots = np.stack([np.stack([perm(41 * (E + u * B + j) + 3) for j in range(B)]) for u in range(R)])
+    drecv = torch.zeros((R * C, H_DX), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm_dx(ctx, torch.from_numpy(cu).to(DEV), dev_u16(dy), dev_u16(w_home),
+                            dev_u16(w_slots), drecv)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    want = oracle.f32_to_bf16(oracle.grouped_gemm_dx(dy, w_home, w_slots, cu, E).astype(np.float32))
+    for u, rho, a, b in ew.segments(cu, E, C):
+        shift = 41 * (rho if rho < E else E + u * B + (rho - E)) + 3
+        cols = (8 * np.arange(H_DX) + shift) % HP_DX
+        np.testing.assert_array_equal(nz(want[a:b]), nz(dy[a:b][:, cols]))
+    np.testing.assert_array_equal(nz(host_u16(drecv)), nz(want))
