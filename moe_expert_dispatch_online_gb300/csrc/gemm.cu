@@ -13,20 +13,25 @@
 //   DX   dRecv[seg] = dY[seg] @ W(u,rho)^T          A: dY, K-major    B: W^T, K-major
 //   DW   dW(u,rho) += recv[seg]^T @ dY[seg] (fp32)  A: recv^T, MN-major  B: dY, MN-major
 //        dW of a home row accumulates into g_home[rho], of slot j into red[u][j].
+// FWD2 / DX2 are FWD / DX with two 128-row m-tiles per unit sharing each weight stage;
+// they run the segments of 2,048 rows or more in a launch of their own before the
+// FWD / DX launch that runs the others (large batches with K >= 2,048 and N tiles of 256).
+// There both TMEM accumulators belong to one unit: the epilogue frees the first before it
+// drains the second, and the MMA thread starts the next unit's first m-tile meanwhile.
 //
 // Design (one GB300):
 //   * a one-CTA prep kernel turns cu_seqlens [R, E+B+1] into a work list on the
-//     device (FWD/DX: m-tiles of 128 rows sharing a weight row; DW: one entry
-//     per non-empty segment), so the host never learns segment sizes;
+//     device (FWD/DX: m-tiles of 128 rows sharing a weight row, FWD2/DX2: 256 rows;
+//     DW: one entry per non-empty segment), so the host never learns segment sizes;
 //   * a persistent kernel, one CTA per SM, strides over work units with the n
 //     tile fastest, so neighbouring CTAs share their A tile in L2;
-//   * warp 0 issues TMA loads (128-byte swizzle) into a 4-stage shared-memory
-//     ring guarded by mbarriers;
+//   * warp 0 issues TMA loads (128-byte swizzle) into a shared-memory ring guarded
+//     by mbarriers (4 stages of 48 KB; FWD2/DX2: 3 stages of 64 KB);
 //   * warp 1 (lane 0) issues tcgen05.mma.kind::f16 (M=128, N=BN<=256, K=16,
 //     bf16 in, fp32 accumulate; M=64 for a FWD/DX m-tile of at most 64 rows) into
 //     one of two TMEM accumulators; tcgen05.commit frees each stage and publishes
 //     each finished tile;
-//   * 4 (DW: 8) epilogue warps drain the other accumulator with tcgen05.ld:
+//   * 4 (DW, FWD2, DX2: 8) epilogue warps drain the other accumulator with tcgen05.ld:
 //     FWD/DX round to bf16 (nearest even) and store only the rows inside the
 //     segment; DW adds the fp32 tile into the gradient rows;
 //   * DW only: a segment's last K block usually extends past the segment, into
