@@ -14,7 +14,7 @@
 //   DW   dW(u,rho) += recv[seg]^T @ dY[seg] (fp32)  A: recv^T, MN-major  B: dY, MN-major
 //        dW of a home row accumulates into g_home[rho], of slot j into red[u][j].
 // FWD2 / DX2 are FWD / DX with two 128-row m-tiles per unit sharing each weight stage;
-// they run the segments of 2,048 rows or more in a launch of their own before the
+// they run the segments of 768 rows or more in a launch of their own before the
 // FWD / DX launch that runs the others (large batches with K >= 2,048 and N tiles of 256).
 // There both TMEM accumulators belong to one unit: the epilogue frees the first before it
 // drains the second, and the MMA thread starts the next unit's first m-tile meanwhile.
@@ -432,7 +432,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 //   segments hold fewer than 256 rows); merged evenly, CTAs on short segments move
 //   gradients while the others keep the tensor pipes busy.
 constexpr int kDwShortRows = 1024;
-constexpr int kDualMinRows = 2048;
+constexpr int kDualMinRows = 768;
 
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ cu, Dims d,
                                                           Workspace ws, int seg_mode) {
@@ -654,11 +654,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 const int brow0 = (p.vm ? u.t.pad : (u.t.wsel >= 0 ? u.t.wsel : (-1 - u.t.wsel))) * p.H;
                 if (MODE == kFwd || MODE == kFwd2) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
-                    if (CF::kDual && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
+                    if (CF::kDual) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
                     for (int c = 0; c < BN / 64; ++c) op(tmB, 2 + c, n0 + c * 64, brow0 + kb * kBK);
                 } else if (MODE == kDx || MODE == kDx2) {
                     op(&tmA, 0, kb * kBK, u.t.row0);
-                    if (CF::kDual && u.t.rows > kBM) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
+                    if (CF::kDual) op(&tmA, 1, kb * kBK, u.t.row0 + kBM);
                     op(tmB, 2, kb * kBK, brow0 + n0);
                 } else {
                     const int r0 = u.t.row0 + kb * kBK;
@@ -680,14 +680,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
             for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
                 const Unit u = unit_at<MODE>(p, unit, NT);
                 const bool rev = (MODE == kFwd || MODE == kFwd2) && (it & 1);
-                const uint32_t ubytes =
-                    (CF::kDual && u.t.rows <= kBM) ? stage_bytes - (uint32_t)kABytes : stage_bytes;
                 for (int kb = 0; kb < u.kb_n; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, status)) {
                         live = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], ubytes);
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
                     ++pr_armed;
                     uint8_t* a_dst = smA + s * kAStage;
                     uint8_t* b_dst = smB + s * b_bytes;
@@ -712,7 +710,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         // both operand tiles by all 32 lanes (whole 128-byte rows, so the
         // swizzle does not matter) before lane 0 issues the MMAs.
         // FWD/DX: an m-tile of at most 64 rows (a segment's last) runs M=64 MMAs, which
-        // put row r of the accumulator in TMEM lane 32 * (r / 16) + r % 16
+        // put row r of the accumulator in TMEM lane 32 * (r / 16) + r % 16.
+        // FWD2/DX2: every unit runs both m-tiles at M=128, whatever its rows. A segment's
+        // odd last m-tile is paired with the rows that follow it (the next segment's, or
+        // the tensor's out-of-bounds zeros), whose results the epilogue never stores.
+        // All units then take the same time, so the CTAs stay in lockstep, and the units
+        // that share a receive-row or weight tile read each K block of it together, while
+        // L2 holds it. With units of two lengths the CTAs drift apart over a launch, and
+        // on the S=8192, E=384 workload at maxvio 0.2 (segments of ~1,400 rows) the launch
+        // read 40 GB from DRAM instead of 21.
         const uint32_t idesc_full = idesc_bf16(kBM, BN, CF::kAmn, CF::kBmn);
         const uint32_t idesc_half = idesc_bf16(kBM / 2, BN, CF::kAmn, CF::kBmn);
         uint32_t s = 0, ph = 0;
@@ -720,24 +726,22 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
         int it = 0;
         for (int unit = blockIdx.x; unit < total && live; unit += gridDim.x, ++it) {
             const Unit u = unit_at<MODE>(p, unit, NT);
-            const uint32_t idesc = (MODE != kDw && u.t.rows <= kBM / 2) ? idesc_half : idesc_full;
+            const uint32_t idesc =
+                (MODE != kDw && !CF::kDual && u.t.rows <= kBM / 2) ? idesc_half : idesc_full;
             // dual modes: both accumulators belong to one unit (m-tile 0 in the first, m-tile
-            // 1, if the unit has one, in the second), so units alternate on one barrier pair
+            // 1 in the second), so units alternate on one barrier pair
             const int acc = CF::kDual ? 0 : it & 1;
             const uint32_t aph = CF::kDual ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
-            const bool two = CF::kDual && u.t.rows > kBM;
-            const uint32_t idesc1 = (u.t.rows - kBM <= kBM / 2) ? idesc_half : idesc_full;
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1u, s_abort, status))) break;
             tc_fence_after();
             const uint32_t dt = tmem_base + (uint32_t)(acc * acc_stride);
             const uint32_t dt1 = tmem_base + (uint32_t)acc_stride;
             int kb = 0;
-            if (CF::kDual && two) {
+            if (CF::kDual) {
                 // The epilogue frees the first accumulator before it drains the second:
                 // run the first m-tile's MMAs over the stages already in the ring (up to all
                 // of them) while the second accumulator is drained, then the second m-tile's
-                // on the same stages, and only then release those stages. A unit of one
-                // m-tile needs only the first accumulator and takes the plain loop.
+                // on the same stages, and only then release those stages.
                 const int pre = min(kStages, u.kb_n);
                 uint32_t s0 = s, ph0 = ph;
                 for (int j = 0; j < pre && live; ++j) {
@@ -770,7 +774,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
                             mma_bf16(dt1, operand_desc<CF::kAmn>(a1, kk), operand_desc<CF::kBmn>(b0, kk),
-                                     idesc1, (j | kk) != 0);
+                                     idesc_full, (j | kk) != 0);
                         mma_commit(&empty[s]);
                     }
                     __syncwarp();
@@ -814,9 +818,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                         if (kk < ksteps) {
                             mma_bf16(dt, operand_desc<CF::kAmn>(a0, kk), operand_desc<CF::kBmn>(b0, kk),
                                      idesc, (kb | kk) != 0);
-                            if (two)
+                            if (CF::kDual)
                                 mma_bf16(dt1, operand_desc<CF::kAmn>(a0 + kABytes, kk),
-                                         operand_desc<CF::kBmn>(b0, kk), idesc1, (kb | kk) != 0);
+                                         operand_desc<CF::kBmn>(b0, kk), idesc_full, (kb | kk) != 0);
                         }
                     mma_commit(&empty[s]);
                 }
@@ -889,14 +893,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1) grouped_gemm_kerne
                 // four whole 128-byte lines), skipping the rows past the segment end, which
                 // belong to the next segment's tile. Two boxes per warp alternate, so one
                 // store can be in flight while the next box is filled.
-                // this warp's rows: 32q..32q+31 of a full tile, or, of an M=64 tile,
+                // this warp's rows: 32q..32q+31 of a full tile, or, of an M=64 tile (FWD/DX),
                 // 16q..16q+15 in lanes 0-15 of its quadrant; a dual unit drains its first
-                // m-tile from the first accumulator, then its second from the second
+                // m-tile from the first accumulator, then its second from the second (none of
+                // whose rows may lie in the segment)
                 for (int half = 0; half < (CF::kDual ? 2 : 1); ++half) {
                 const int trows = CF::kDual ? min(u.t.rows - half * kBM, kBM) : u.t.rows;
                 const int trow0 = u.t.row0 + half * kBM;
                 const uint32_t tb = tbase + (uint32_t)(half * acc_stride);
-                const int wrows = trows <= kBM / 2 ? 16 : 32;
+                const int wrows = (!CF::kDual && trows <= kBM / 2) ? 16 : 32;
                 const int nvalid = min(wrows, trows - q * wrows);   // of them inside the segment
                 const int rsub = lane >> 3, piece = lane & 7;
                 const int orow = trow0 + q * wrows;

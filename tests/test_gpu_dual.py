@@ -1,12 +1,14 @@
 """The forward GEMM's two-m-tile units, on hand-made cu_seqlens tables.
 
-Segments of 2,048 rows or more run in a launch of their own with two 128-row
-m-tiles per unit sharing each weight stage (the second m-tile of a unit may be
-ragged, down to one row, or absent), the other segments in the usual one-m-tile
-launch. These tables mix both kinds with every tail case: an even number of
-m-tiles, an odd number (the last unit holds one m-tile), a second m-tile of at
-most 64 rows (M=64 MMAs), a first m-tile of at most 64 rows, and short
-segments. Compared with the binary64 oracle in full (relative Frobenius per
+Segments of 768 rows or more run in a launch of their own with two 128-row
+m-tiles per unit sharing each weight stage; the other segments run in the usual
+one-m-tile launch. Every two-m-tile unit runs both m-tiles at M=128: a unit's
+second m-tile may be ragged, down to one row, or lie wholly past the segment end,
+on rows whose results are never stored (the next segment's, or past the end of
+the tensor). These tables mix both kinds with every tail case: an even number of
+m-tiles, an odd number (the last unit's second m-tile lies past the segment), a
+second m-tile of at most 64 rows, a first m-tile of at most 64 rows, a segment
+that ends at the end of the tensor, and short segments. Compared with the binary64 oracle in full (relative Frobenius per
 segment and every element against the fp32-accumulation bound), exactly with
 permutation weights, rows outside every segment untouched, and the
 two-pointer GEMM equal bit for bit to the VM GEMM on materialised views. The
@@ -26,9 +28,10 @@ RTOL = 2e-2
 
 # R=2, E=4 (2 home experts per rank), B=2, K=2, S=4096: C=8192 rows per rank.
 # H=2048 (the reduction length) and H'=256 (one 256-column tile): the conditions
-# under which the two-m-tile launch runs.
+# under which the two-m-tile launch runs. MIN_ROWS is its threshold.
 R, E, B, K, S, H, HP = 2, 4, 2, 2, 4096, 2048, 256
 C = S * K
+MIN_ROWS = 768
 LENGTHS = [
     [2048, 2177, 1500, 2100, 300, 64],      # 16 m-tiles; 1-row second tile; short; 52-row unit
     [2113, 2276, 0, 1, 1752, 2050],         # 65-row one-tile unit; 100-row second tile; 1; 2-row unit
@@ -69,11 +72,14 @@ def covered(cu):
 def test_lengths_reach_both_launches():
     assert table()[:, -1].max() <= C
     flat = [n for row in LENGTHS for n in row if n > 0]
-    assert any(n >= 2048 and (n + 127) // 128 % 2 == 0 for n in flat)     # even m-tile count
-    assert any(n >= 2048 and (n + 127) // 128 % 2 == 1 for n in flat)     # odd: a one-m-tile unit
-    assert any(n >= 2048 and 0 < n % 256 - 128 <= 64 for n in flat)       # second m-tile <= 64 rows
-    assert any(n >= 2048 and 0 < n % 256 <= 64 for n in flat)             # first m-tile <= 64 rows
-    assert any(0 < n < 2048 for n in flat)                                # the one-m-tile launch
+    long_ = [n for n in flat if n >= MIN_ROWS]
+    assert any((n + 127) // 128 % 2 == 0 for n in long_)     # even m-tile count
+    assert any((n + 127) // 128 % 2 == 1 for n in long_)     # odd: a second m-tile past the segment
+    assert any(0 < n % 256 - 128 <= 64 for n in long_)       # second m-tile <= 64 rows
+    assert any(0 < n % 256 <= 64 for n in long_)             # first m-tile <= 64 rows
+    assert any(MIN_ROWS <= n < 2048 for n in long_)          # long, below the earlier 2,048 threshold
+    assert any(0 < n < MIN_ROWS for n in flat)               # the one-m-tile launch
+    assert table()[-1, -1] == C and LENGTHS[-1][-1] >= MIN_ROWS   # ends at the end of the tensor
 
 
 def test_forward_two_mtile_units_against_binary64(lib):
