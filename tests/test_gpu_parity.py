@@ -443,6 +443,56 @@ def test_grouped_gemm_bench_size_sampled(lib, name, target):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("target", (0.2, 20.0))
+def test_second_projection_bench_size_sampled(lib, target):
+    """The down projection ([E+B, H', H], a second context with H and H' swapped) at the
+    S=8192, E=384 size, on the same plan: K = H' = 2048 and N = H = 7168, so its long
+    segments run the two-m-tile launch with 28 N tiles each. Sampled rows of chosen segments
+    (every rank's first and last, and two remote ones) against the oracle, all columns."""
+    bep = lib
+    _cache.clear()
+    torch.cuda.empty_cache()
+    wl = synth.WORKLOADS["bench_r8_e384"]
+    topk = synth.routing(wl, target, 0)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert_plan_equal(buf, ref)
+    C, E = wl.C, wl.E
+    ctx2 = bep.Context(bep.Config(wl.R, E, wl.B, wl.K, wl.S, wl.Hp, wl.H, wl.mode))
+    y1 = synth.tokens_device((wl.R * C, wl.Hp), 31)
+    w_dn = synth.weights_device((E, wl.Hp, wl.H), 32)
+    dn_slots = torch.zeros((wl.R, wl.B, wl.Hp, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx2, buf.slot_expert, w_dn, dn_slots)
+    y2 = torch.empty((wl.R * C, wl.H), dtype=torch.bfloat16, device=DEV)
+    bep.bep_grouped_gemm(ctx2, buf.cu_seqlens, y1, w_dn, dn_slots, y2)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx2) == 0
+    rng = np.random.default_rng(3)
+    checked = 0
+    worst = ew.Worst()
+    for u in range(wl.R):
+        segs = [rho for rho in range(E + wl.B) if ref.cu[u, rho + 1] > ref.cu[u, rho]]
+        remote = [rho for rho in segs if rho >= E or rho // (E // wl.R) != u]
+        for rho in sorted(set(segs[:1] + segs[-1:] + remote[:2])):
+            a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+            rows = sorted(set([a, b - 1] + list(rng.integers(a, b, size=2))))
+            gi = torch.from_numpy(np.array([u * C + r for r in rows], np.int64)).to(DEV)
+            a_rows = host_u16(y1[gi])
+            w = host_u16(w_dn[oracle.weight_row_of(rho, u, E, ref.slot_expert)])
+            yr = oracle.gemm_rows(a_rows, w)
+            yg = oracle.bf16_to_f32(host_u16(y2[gi])).astype(np.float64)
+            err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
+            assert err <= GEMM_RTOL, (u, rho, err)
+            A = oracle.bf16_to_f32(a_rows).astype(np.float64)
+            W = oracle.bf16_to_f32(w).astype(np.float64)
+            worst.add(ew.fwd(yg, yr, A, W, f"rank {u} row {rho}"), err)
+            checked += len(rows)
+    assert checked > 0
+    print(f"second projection {target}: {checked} rows; {worst}")
+    del y1, w_dn, dn_slots, y2
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------- whole path
 def test_forward_and_backward_fold_in_one_stream_graph(lib):
     """Capture plan -> prefetch -> dispatch -> GEMM -> combine -> combine_bwd in a
