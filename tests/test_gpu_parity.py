@@ -443,6 +443,61 @@ def test_grouped_gemm_bench_size_sampled(lib, name, target):
     torch.cuda.empty_cache()
 
 
+def test_grouped_gemm_large_inference_batch_sampled(lib):
+    """An inference plan (B=4 < E/R) on a batch large enough for the two-m-tile launch
+    (S=8192, about 1,365 rows per expert): its overflow segments, which read their weight
+    rows in place from other ranks' home rows, hold thousands of rows and run two m-tiles
+    per unit. The plan must be bit-exact; then sampled rows of every overflow segment and of
+    each rank's first, last and slot segments against the oracle, all columns."""
+    bep = lib
+    _cache.clear()
+    torch.cuda.empty_cache()
+    wl = synth.Workload("infer_r8_e384_b4_s8192", R=8, S=8192, E=384, K=8, H=7168, Hp=2048, B=4,
+                        mode=synth.MODE_INFER)
+    topk = synth.gumbel_topk(wl.R, wl.S, wl.K, synth.zipf_popularity(wl.E, 1.2), 0)
+    ref = oracle.plan(topk, wl.E, wl.B, wl.mode)
+    C, E, G = wl.C, wl.E, wl.E // wl.R
+    overflow = [(u, rho) for u in range(wl.R) for rho in range(E)
+                if ref.cu[u, rho + 1] > ref.cu[u, rho] and rho // G != u]
+    assert overflow and min(int(ref.cu[u, rho + 1] - ref.cu[u, rho]) for u, rho in overflow) >= 768
+    ctx, buf = gpu_plan(bep, cfg_of(bep, wl), topk)
+    assert_plan_equal(buf, ref)
+    x = synth.tokens_device((wl.R, wl.S, wl.H), 41)
+    w_home = synth.weights_device((E, wl.H, wl.Hp), 42)
+    w_slots = torch.zeros((wl.R, wl.B, wl.H, wl.Hp), dtype=torch.bfloat16, device=DEV)
+    bep.bep_prefetch_weight(ctx, buf.slot_expert, w_home, w_slots)
+    bep.bep_dispatch(ctx, x, buf.dest, buf.recv)
+    bep.bep_grouped_gemm(ctx, buf.cu_seqlens, buf.recv, w_home, w_slots, buf.y)
+    torch.cuda.synchronize()
+    assert bep.bep_status(ctx) == 0
+    inv = np.empty(wl.R * C, np.int64)
+    inv[ref.dest.ravel()] = np.arange(wl.R * wl.S * wl.K) // wl.K
+    rng = np.random.default_rng(4)
+    picks = set(overflow)
+    for u in range(wl.R):
+        segs = [rho for rho in range(E + wl.B) if ref.cu[u, rho + 1] > ref.cu[u, rho]]
+        picks.update((u, rho) for rho in segs[:1] + segs[-1:] + [r for r in segs if r >= E][:2])
+    checked = 0
+    worst = ew.Worst()
+    for u, rho in sorted(picks):
+        a, b = int(ref.cu[u, rho]), int(ref.cu[u, rho + 1])
+        rows = sorted(set([a, b - 1] + list(rng.integers(a, b, size=2))))
+        gi = np.array([u * C + r for r in rows], np.int64)
+        a_rows = host_u16(x.view(-1, wl.H)[torch.from_numpy(inv[gi]).to(DEV)])
+        w = host_u16(w_home[oracle.weight_row_of(rho, u, E, ref.slot_expert)])
+        yr = oracle.gemm_rows(a_rows, w)
+        yg = oracle.bf16_to_f32(host_u16(buf.y[torch.from_numpy(gi).to(DEV)])).astype(np.float64)
+        err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
+        assert err <= GEMM_RTOL, (u, rho, err)
+        A = oracle.bf16_to_f32(a_rows).astype(np.float64)
+        W = oracle.bf16_to_f32(w).astype(np.float64)
+        worst.add(ew.fwd(yg, yr, A, W, f"rank {u} row {rho}"), err)
+        checked += len(rows)
+    print(f"large inference batch: {len(overflow)} overflow segments, {checked} rows; {worst}")
+    del w_home, w_slots, x
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("target", (0.2, 20.0))
 def test_second_projection_bench_size_sampled(lib, target):
     """The down projection ([E+B, H', H], a second context with H and H' swapped) at the
